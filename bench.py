@@ -1,0 +1,407 @@
+"""Benchmark of the thread-block-cluster histogram on one GB300 (or N replicas).
+
+One step = one whole histogram of the workload's keys: the cluster kernel
+(zero slices, stream keys, DSMEM increments, flush partial rows) followed by
+the partial-row reduction, both launched through the library's C ABI.  Keys
+are resident in HBM when the timed region starts; the 1 GiB input is larger
+than the 129 MB L2, so no flush is needed between steps.
+
+Prints ONE JSON line on rank 0.  Under torchrun (N > 1) every rank runs an
+independent replica on its own GPU with its own seed (weak scaling; there is
+no collective on the data path) and the slowest rank's time is reported.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the CPU oracle as the reference arm
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "keys/s and achieved HBM GB/s vs GB300 peak (1 GPU), bit-exact vs CPU oracle"
+UNIT = "keys/s"
+DEFAULT_WORKLOAD = "uniform-256M-256K"
+# Cluster size each synthetic workload is published with.
+WORKLOAD_CLUSTER = {
+    "uniform-1M-8K": 2,
+    "uniform-64M-64K": 2,
+    "uniform-256M-256K": 8,
+    "zipf1.1-256M-256K": 8,
+    "runs256-1G-512K": 16,
+}
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+L2_BYTES = 129 * 1024 * 1024
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "cluster_hist_traffic.json")
+KERNEL_SOURCE = os.path.join(ROOT, "cluster_distributed_shared_gb300", "csrc", "cluster_hist.cu")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOAD_CLUSTER))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    a = ap.parse_args()
+    if a.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if a.steps < 1:
+        ap.error("--steps must be >= 1")
+    return a
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def workload_config(name, seed):
+    import gen
+    w = gen.WORKLOADS[name]
+    return {
+        "workload": name,
+        "n": w["n"],
+        "num_bins": w["num_bins"],
+        "distribution": w["dist"],
+        "seed": seed,
+        "cluster_size": WORKLOAD_CLUSTER[name],
+        "l2": "inputs larger than L2 (no flush)" if 4 * w["n"] > L2_BYTES
+        else "inputs L2-resident (smaller than L2; no flush)",
+    }
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.lines = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [l for (t, l) in self.lines if t0 - 0.06 <= t <= t1 + 0.06] or \
+               [l for (_, l) in self.lines]
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {
+            "sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(smax) if smax else None,
+            "power_w_max": max(power) if power else None,
+            "samples": len(sm),
+            "reasons": sorted(reasons),
+        }
+
+
+def gpu_id_for(torch, dev_index):
+    try:
+        u = str(torch.cuda.get_device_properties(dev_index).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        return vis.split(",")[dev_index] if vis else str(dev_index)
+
+
+# ---------------------------------------------------------------- peaks
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_traffic(n_keys, num_bins, cluster_size):
+    """Per-launch DRAM bytes of the cluster kernel from the committed ncu
+    summary, scaled to this launch's keys; None when the kernel source has
+    changed since the counters were taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+        with open(KERNEL_SOURCE, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+    except (OSError, ValueError):
+        return None
+    if rec.get("kernel_source_sha256") != sha:
+        return None
+    for e in rec.get("captures", []):
+        if e.get("num_bins") == num_bins and e.get("cluster_size") == cluster_size:
+            return e["dram_bytes"] * (n_keys / e["n"])
+    return None
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(a, world, rank):
+    if rank != 0:
+        return
+    import gen
+    import oracle
+    cfg = workload_config(a.workload, a.seed)
+    keys = gen.workload(a.workload, a.seed)
+    n, num_bins = cfg["n"], cfg["num_bins"]
+    # Size each step's sample so the whole run stays around a minute.
+    probe = keys[: 1 << 20]
+    t0 = time.perf_counter()
+    oracle.histogram(probe, num_bins)
+    t_key = max((time.perf_counter() - t0) / probe.size, 1e-10)
+    sample = int(min(n, max(1 << 16, 40.0 / ((a.steps + a.warmup) * t_key))))
+    sample -= sample % 4096 or 0
+    sample = max(sample, 4096)
+    out = np.empty(num_bins, np.uint32)
+    chunks = max(1, n // sample)
+    for k in range(a.warmup):
+        o = (k % chunks) * sample
+        oracle.histogram(keys[o:o + sample], num_bins, out)
+    t0 = time.perf_counter()
+    for k in range(a.steps):
+        o = (k % chunks) * sample
+        oracle.histogram(keys[o:o + sample], num_bins, out)
+    dt = time.perf_counter() - t0
+    value = sample * a.steps / dt
+    desc = (f"{sample} contiguous keys of the {n}-key workload per step, cycling through it; "
+            "single-threaded C loop")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": 1e3 * dt / a.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
+        "data": "synthetic (seeded generator)", "config": cfg,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(a, world, rank, local):
+    import torch
+    import cluster_distributed_shared_gb300 as pkg
+    import gen
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    cfg = workload_config(a.workload, a.seed)
+    seed = a.seed + rank
+    n, num_bins, P = cfg["n"], cfg["num_bins"], cfg["cluster_size"]
+    keys_h = gen.workload(a.workload, seed)
+    keys = torch.from_numpy(keys_h).to(dev)
+    plan = pkg.dsmem_hist_plan(num_bins, n, cluster_size=P)
+    partials = torch.empty(plan["num_clusters"] * plan["partial_stride"], dtype=torch.int32,
+                           device=dev)
+    bins = torch.empty(num_bins, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        pkg.dsmem_hist_partials(keys, num_bins, plan, partials, 0, stream)
+        pkg.dsmem_hist_reduce(partials, plan["num_clusters"], plan["partial_stride"], num_bins,
+                              bins, stream)
+
+    for _ in range(a.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    # Parity of the benchmarked configuration (rank 0 at N = 1 compares with
+    # the oracle; the oracle run doubles as the CPU baseline).
+    parity = None
+    cpu = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        import oracle
+        med, reps = oracle.time_histogram(keys_h, num_bins, min_seconds=a.cpu_seconds)
+        want = oracle.histogram(keys_h, num_bins)
+        got = bins.cpu().numpy().view(np.uint32)
+        parity = "bit-exact vs oracle" if np.array_equal(got, want) else \
+            f"MISMATCH in {int((got != want).sum())} bins"
+        cpu = {"value": n / med, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"full {n}-key workload (seed {seed}), median of {reps} runs"}
+
+    sampler = ClockSampler(gpu_id_for(torch, local))
+    sampler.start()
+    ev_start = torch.cuda.Event(enable_timing=True)
+    ev_end = torch.cuda.Event(enable_timing=True)
+    ev_k = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(a.steps)]
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    t_host0 = time.perf_counter()
+    ev_start.record(stream)
+    for k in range(a.steps):
+        ev_k[k][0].record(stream)
+        pkg.dsmem_hist_partials(keys, num_bins, plan, partials, 0, stream)
+        ev_k[k][1].record(stream)
+        pkg.dsmem_hist_reduce(partials, plan["num_clusters"], plan["partial_stride"], num_bins,
+                              bins, stream)
+    ev_end.record(stream)
+    torch.cuda.synchronize(dev)
+    t_host1 = time.perf_counter()
+    if pg:
+        pg.barrier()
+    clocks = sampler.stop(t_host0, t_host1)
+    ms_total = ev_start.elapsed_time(ev_end)
+    kernel_ms = [s.elapsed_time(e) for s, e in ev_k]
+    cluster_ms = sum(kernel_ms) / len(kernel_ms)
+    if pg:
+        t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / a.steps
+    value = world * n * a.steps / (ms_total / 1e3)
+
+    # The global-atomics comparison kernel, timed the same way on the same keys.
+    cmp_steps = max(1, min(a.steps, 50))
+    for _ in range(3):
+        pkg.dsmem_hist_global_atomic(keys, num_bins, out=bins, stream=stream)
+    torch.cuda.synchronize(dev)
+    ev_start.record(stream)
+    for _ in range(cmp_steps):
+        pkg.dsmem_hist_global_atomic(keys, num_bins, out=bins, stream=stream)
+    ev_end.record(stream)
+    torch.cuda.synchronize(dev)
+    ga_ms = ev_start.elapsed_time(ev_end) / cmp_steps
+    comparison = {"kernel": "global_atomic_hist_kernel (one global atomic per key)",
+                  "ms_per_step": ga_ms, "value": n / (ga_ms / 1e3), "unit": UNIT,
+                  "steps": cmp_steps}
+
+    # End to end through the host-buffer entry point: pinned keys in, the
+    # histogram back in host memory, every step.
+    e2e = None
+    if not a.no_e2e:
+        keys_pin = torch.from_numpy(keys_h).pin_memory()
+        out_pin = torch.empty(num_bins, dtype=torch.int32).pin_memory()
+        pkg.dsmem_hist_host(keys_pin, num_bins, out=out_pin)  # warm the staging pool
+        e2e_steps = max(1, min(a.e2e_steps, a.steps))
+        if pg:
+            pg.barrier()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            pkg.dsmem_hist_host(keys_pin, num_bins, out=out_pin)
+        dt = time.perf_counter() - t0
+        if pg:
+            t = torch.tensor([dt], dtype=torch.float64, device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            dt = float(t.item())
+        ok = parity is None or np.array_equal(out_pin.numpy().view(np.uint32), want)
+        e2e = {"value": world * n * e2e_steps / dt, "unit": UNIT,
+               "h2d_bytes_per_step": 4 * n, "d2h_bytes_per_step": 4 * num_bins,
+               "steps": e2e_steps, "call": "dsmem_hist_host (pinned host keys -> host bins)",
+               "parity": "bit-exact vs oracle" if ok else "MISMATCH"}
+        del keys_pin, out_pin
+
+    peak, peak_src = hbm_peak()
+    alg_bytes = 4 * n + 4 * num_bins
+    achieved = alg_bytes / (cluster_ms / 1e3) / 1e9
+    traffic = kernel_traffic(n, num_bins, P)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int32", "data": "synthetic (seeded generator)",
+        "config": cfg,
+        "plan": plan,
+        "achieved_gbs": world * alg_bytes / (ms_step / 1e3) / 1e9,
+        "pct_of_nominal_8tbs": 100.0 * (alg_bytes / (ms_step / 1e3) / 1e9) / NOMINAL_HBM_GBS,
+        "roofline": {"bound": "hbm", "kernel": "cluster_hist_kernel", "achieved": achieved,
+                     "peak": peak, "peak_source": peak_src, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "algorithmic_bytes": alg_bytes, "avg_launch_ms": cluster_ms,
+                     "share_of_step": cluster_ms / ms_step},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "global_atomic_comparison": comparison,
+        "gpu_launches": 2 * a.steps,
+        "clocks": clocks,
+        "parity": parity,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+def main():
+    a = parse()
+    world, rank, local = dist_env()
+    if a.impl == "reference":
+        run_reference(a, world, rank)
+    else:
+        run_ours(a, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,493 @@
+// C ABI of libdsmemhist: argument checks, per-device state, scratch from a
+// stream-ordered memory pool, and the launch sequence
+//   cluster_hist_kernel  (zero slices, stream keys, DSMEM increments, flush)
+//   reduce_partials      (sum the clusters' partial rows into `bins`).
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+
+#include <cuda_runtime_api.h>
+
+#include "dsmem_hist.h"
+#include "internal.h"
+
+namespace dsmh {
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int fail_cuda(cudaError_t e, const char* what) {
+  return fail(DSMEM_HIST_ECUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+struct DeviceState {
+  bool ready = false;
+  dsmem_hist_device_t dev = {};
+  cudaMemPool_t pool = nullptr;
+  cudaStream_t copy_stream = nullptr;
+  cudaEvent_t ev_copied[2] = {nullptr, nullptr};
+  cudaEvent_t ev_consumed[2] = {nullptr, nullptr};
+  int prepared_smem[2] = {0, 0};  // largest dynamic smem set per kernel variant
+  // (aggregate, P, threads, smem) -> resident clusters
+  std::map<std::tuple<int, int, int, int>, int> occupancy;
+  std::mutex host_call;  // serialises dsmem_hist_host on this device
+};
+
+std::mutex g_mutex;
+std::map<int, DeviceState*> g_devices;
+
+bool trace_enabled() {
+  static int on = -1;
+  if (on < 0) {
+    const char* v = getenv("DSMEM_HIST_TRACE");
+    on = (v && *v && strcmp(v, "0") != 0) ? 1 : 0;
+  }
+  return on == 1;
+}
+
+int env_int(const char* name, int fallback) {
+  const char* v = getenv(name);
+  if (!v || !*v) return fallback;
+  return atoi(v);
+}
+
+// Per-device state for the current device; g_mutex must be held.
+int device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  DeviceState*& st = g_devices[dev];
+  if (!st) st = new DeviceState();
+  if (!st->ready) {
+    cudaDeviceProp p;
+    if ((e = cudaGetDeviceProperties(&p, dev)) != cudaSuccess)
+      return fail_cuda(e, "cudaGetDeviceProperties");
+    st->dev.cc_major = p.major;
+    st->dev.cc_minor = p.minor;
+    st->dev.sm_count = p.multiProcessorCount;
+    st->dev.max_smem_per_block_optin = static_cast<int32_t>(p.sharedMemPerBlockOptin);
+    st->dev.max_smem_per_sm = static_cast<int32_t>(p.sharedMemPerMultiprocessor);
+    st->dev.max_threads_per_sm = p.maxThreadsPerMultiProcessor;
+    int cluster_launch = 0;
+    cudaDeviceGetAttribute(&cluster_launch, cudaDevAttrClusterLaunch, dev);
+    st->dev.max_cluster_size = (p.major >= 9 && cluster_launch) ? 16 : 1;
+    st->ready = true;
+  }
+  *out = st;
+  return DSMEM_HIST_OK;
+}
+
+int ensure_pool(DeviceState* st) {
+  if (st->pool) return DSMEM_HIST_OK;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaMemPoolProps props = {};
+  props.allocType = cudaMemAllocationTypePinned;
+  props.location.type = cudaMemLocationTypeDevice;
+  props.location.id = dev;
+  cudaError_t e = cudaMemPoolCreate(&st->pool, &props);
+  if (e != cudaSuccess) {
+    st->pool = nullptr;
+    return fail_cuda(e, "cudaMemPoolCreate");
+  }
+  // Keep freed scratch in the pool between calls instead of returning it to
+  // the driver at every synchronisation.
+  uint64_t keep = UINT64_MAX;
+  cudaMemPoolSetAttribute(st->pool, cudaMemPoolAttrReleaseThreshold, &keep);
+  return DSMEM_HIST_OK;
+}
+
+// Plans for the current device, confirming the shape with the occupancy
+// API; in automatic mode a cluster size the device cannot hold is halved
+// (more passes) until one fits.  g_mutex must be held.
+int plan_locked(DeviceState* st, int32_t num_bins, int64_t n, const dsmem_hist_request_t* req_in,
+                dsmem_hist_plan_t* out) {
+  dsmem_hist_request_t req = {0, 0, 0, -1, 0};
+  if (req_in) req = *req_in;
+  // Environment overrides for sweeps (only where the caller left a field open).
+  if (req.cluster_size == 0) req.cluster_size = env_int("DSMEM_HIST_CLUSTER", 0);
+  if (req.block_threads == 0) req.block_threads = env_int("DSMEM_HIST_BLOCK", 0);
+  if (req.num_clusters == 0) req.num_clusters = env_int("DSMEM_HIST_GRID", 0);
+  if (req.aggregate < 0) req.aggregate = env_int("DSMEM_HIST_AGGREGATE", -1);
+
+  dsmem_hist_device_t dev = st->dev;
+  for (;;) {
+    const char* why = "";
+    int rc = plan_shape(&dev, num_bins, n, &req, 0, out, &why);
+    if (rc != DSMEM_HIST_OK) return fail(rc, "plan: %s", why);
+    cudaError_t e;
+    const int agg = out->aggregate;
+    if (out->smem_bytes > st->prepared_smem[agg]) {
+      if ((e = prepare_cluster_kernel(agg, out->smem_bytes)) != cudaSuccess)
+        return fail_cuda(e, "cudaFuncSetAttribute");
+      st->prepared_smem[agg] = out->smem_bytes;
+    }
+    auto key = std::make_tuple(agg, out->cluster_size, out->block_threads, out->smem_bytes);
+    auto it = st->occupancy.find(key);
+    int mac = 0;
+    if (it != st->occupancy.end()) {
+      mac = it->second;
+    } else {
+      e = query_max_active_clusters(agg, out->cluster_size, out->block_threads, out->smem_bytes,
+                                    &mac);
+      if (e != cudaSuccess) {
+        cudaGetLastError();  // clear the sticky-free error of a refused shape
+        mac = 0;
+      }
+      st->occupancy[key] = mac;
+    }
+    if (mac > 0) {
+      rc = plan_shape(&dev, num_bins, n, &req, mac, out, &why);
+      if (rc != DSMEM_HIST_OK) return fail(rc, "plan: %s", why);
+      break;
+    }
+    if (req.cluster_size != 0 || out->cluster_size <= 1)
+      return fail(DSMEM_HIST_EUNSUPPORTED,
+                  "cluster of %d CTAs x %d threads x %d B shared memory cannot be resident",
+                  out->cluster_size, out->block_threads, out->smem_bytes);
+    dev.max_cluster_size = out->cluster_size / 2;
+  }
+  if (trace_enabled())
+    fprintf(stderr,
+            "[dsmem_hist] bins=%d n=%lld -> P=%d S=%d passes=%d threads=%d C=%d smem=%d agg=%d "
+            "ctas/SM=%d max_active_clusters=%d scratch=%lld B\n",
+            num_bins, static_cast<long long>(n), out->cluster_size, out->bins_per_cta,
+            out->passes, out->block_threads, out->num_clusters, out->smem_bytes, out->aggregate,
+            out->ctas_per_sm, out->max_active_clusters,
+            static_cast<long long>(out->workspace_bytes));
+  return DSMEM_HIST_OK;
+}
+
+int check_args(const void* keys, int64_t n, int32_t num_bins, const void* bins) {
+  if (n < 0) return fail(DSMEM_HIST_EINVAL, "n must be >= 0 (got %lld)", static_cast<long long>(n));
+  if (num_bins < 1) return fail(DSMEM_HIST_EINVAL, "num_bins must be >= 1 (got %d)", num_bins);
+  if (!bins) return fail(DSMEM_HIST_EINVAL, "bins is NULL");
+  if (n > 0 && !keys) return fail(DSMEM_HIST_EINVAL, "keys is NULL with n > 0");
+  if ((reinterpret_cast<uintptr_t>(keys) & 3u) || (reinterpret_cast<uintptr_t>(bins) & 3u))
+    return fail(DSMEM_HIST_EINVAL, "keys and bins must be 4-byte aligned");
+  return DSMEM_HIST_OK;
+}
+
+uint32_t head_keys(const int32_t* keys, int64_t n) {
+  const uint32_t h = static_cast<uint32_t>(((16u - (reinterpret_cast<uintptr_t>(keys) & 15u)) & 15u) / 4u);
+  return n < h ? static_cast<uint32_t>(n) : h;
+}
+
+ClusterHistArgs make_args(const dsmem_hist_plan_t& plan, const int32_t* keys, int64_t n,
+                          int32_t num_bins, uint32_t* partials, int accumulate) {
+  ClusterHistArgs a;
+  a.keys = keys;
+  a.n = n;
+  a.partials = partials;
+  a.num_bins = static_cast<uint32_t>(num_bins);
+  a.S = static_cast<uint32_t>(plan.bins_per_cta);
+  a.magic = owner_magic(a.S);
+  a.passes = static_cast<uint32_t>(plan.passes);
+  a.stride = static_cast<uint64_t>(plan.partial_stride);
+  a.head = head_keys(keys, n);
+  a.accumulate = static_cast<uint32_t>(accumulate);
+  return a;
+}
+
+int run_device(const int32_t* keys, int64_t n, int32_t num_bins, uint32_t* bins,
+               const dsmem_hist_request_t* req, cudaStream_t stream) {
+  int rc = check_args(keys, n, num_bins, bins);
+  if (rc) return rc;
+  dsmem_hist_plan_t plan;
+  DeviceState* st = nullptr;
+  {
+    std::lock_guard<std::mutex> g(g_mutex);
+    if ((rc = device_state(&st))) return rc;
+    if ((rc = plan_locked(st, num_bins, n, req, &plan))) return rc;
+    if ((rc = ensure_pool(st))) return rc;
+  }
+  cudaError_t e;
+  if (n == 0) {
+    e = cudaMemsetAsync(bins, 0, sizeof(uint32_t) * static_cast<size_t>(num_bins), stream);
+    return e == cudaSuccess ? DSMEM_HIST_OK : fail_cuda(e, "cudaMemsetAsync");
+  }
+  void* scratch = nullptr;
+  e = cudaMallocFromPoolAsync(&scratch, static_cast<size_t>(plan.workspace_bytes), st->pool, stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(DSMEM_HIST_ENOMEM, "scratch pool: %lld bytes: %s",
+                static_cast<long long>(plan.workspace_bytes), cudaGetErrorString(e));
+  }
+  uint32_t* partials = static_cast<uint32_t*>(scratch);
+  const ClusterHistArgs args = make_args(plan, keys, n, num_bins, partials, 0);
+  e = launch_cluster_hist(plan, args, stream);
+  if (e == cudaSuccess)
+    e = launch_reduce_partials(partials, args.stride, static_cast<uint32_t>(plan.num_clusters),
+                               args.num_bins, bins, stream);
+  const cudaError_t ef = cudaFreeAsync(scratch, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "cluster histogram launch");
+  if (ef != cudaSuccess) return fail_cuda(ef, "cudaFreeAsync");
+  return DSMEM_HIST_OK;
+}
+
+// Consistency of a caller-supplied plan with num_bins and the device.
+int check_plan(const DeviceState* st, const dsmem_hist_plan_t* p, int32_t num_bins) {
+  if (!p) return fail(DSMEM_HIST_EINVAL, "plan is NULL");
+  const int64_t P = p->cluster_size, S = p->bins_per_cta;
+  if (P < 1 || P > 16 || P > st->dev.max_cluster_size)
+    return fail(DSMEM_HIST_EINVAL, "plan: cluster_size %lld out of range", static_cast<long long>(P));
+  if (S < 4 || (S & 3) || S >= (int64_t{1} << 18) || p->smem_bytes != 4 * S ||
+      p->smem_bytes > st->dev.max_smem_per_block_optin)
+    return fail(DSMEM_HIST_EINVAL, "plan: bins_per_cta / smem_bytes inconsistent");
+  if (p->passes < 1 || static_cast<int64_t>(p->passes) * P * S < num_bins ||
+      static_cast<int64_t>(p->passes - 1) * P * S >= num_bins)
+    return fail(DSMEM_HIST_EINVAL, "plan: passes do not cover num_bins exactly");
+  if (p->block_threads < 64 || p->block_threads > 1024 || (p->block_threads & 31))
+    return fail(DSMEM_HIST_EINVAL, "plan: block_threads invalid");
+  if (p->num_clusters < 1 || p->aggregate < 0 || p->aggregate > 1)
+    return fail(DSMEM_HIST_EINVAL, "plan: num_clusters / aggregate invalid");
+  if (p->partial_stride < num_bins || (p->partial_stride & 3))
+    return fail(DSMEM_HIST_EINVAL, "plan: partial_stride must be >= num_bins and a multiple of 4");
+  return DSMEM_HIST_OK;
+}
+
+int run_partials(const int32_t* keys, int64_t n, int32_t num_bins, const dsmem_hist_plan_t* plan,
+                 uint32_t* partials, int32_t accumulate, cudaStream_t stream) {
+  int rc = check_args(keys, n, num_bins, partials);
+  if (rc) return rc;
+  if (reinterpret_cast<uintptr_t>(partials) & 15u)
+    return fail(DSMEM_HIST_EINVAL, "partials must be 16-byte aligned");
+  if (accumulate != 0 && accumulate != 1) return fail(DSMEM_HIST_EINVAL, "accumulate must be 0 or 1");
+  {
+    std::lock_guard<std::mutex> g(g_mutex);
+    DeviceState* st = nullptr;
+    if ((rc = device_state(&st))) return rc;
+    if ((rc = check_plan(st, plan, num_bins))) return rc;
+    if (plan->smem_bytes > st->prepared_smem[plan->aggregate]) {
+      const cudaError_t e = prepare_cluster_kernel(plan->aggregate, plan->smem_bytes);
+      if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute");
+      st->prepared_smem[plan->aggregate] = plan->smem_bytes;
+    }
+  }
+  const ClusterHistArgs args = make_args(*plan, keys, n, num_bins, partials, accumulate);
+  const cudaError_t e = launch_cluster_hist(*plan, args, stream);
+  return e == cudaSuccess ? DSMEM_HIST_OK : fail_cuda(e, "cluster histogram launch");
+}
+
+int run_reduce(const uint32_t* partials, int32_t num_clusters, int64_t stride, int32_t num_bins,
+               uint32_t* bins, cudaStream_t stream) {
+  if (num_bins < 1) return fail(DSMEM_HIST_EINVAL, "num_bins must be >= 1");
+  if (!partials || !bins) return fail(DSMEM_HIST_EINVAL, "partials and bins must not be NULL");
+  if (num_clusters < 1) return fail(DSMEM_HIST_EINVAL, "num_clusters must be >= 1");
+  if (stride < num_bins || (stride & 3))
+    return fail(DSMEM_HIST_EINVAL, "partial_stride must be >= num_bins and a multiple of 4");
+  if ((reinterpret_cast<uintptr_t>(partials) & 15u) || (reinterpret_cast<uintptr_t>(bins) & 3u))
+    return fail(DSMEM_HIST_EINVAL, "partials must be 16-byte and bins 4-byte aligned");
+  const cudaError_t e = launch_reduce_partials(partials, static_cast<uint64_t>(stride),
+                                               static_cast<uint32_t>(num_clusters),
+                                               static_cast<uint32_t>(num_bins), bins, stream);
+  return e == cudaSuccess ? DSMEM_HIST_OK : fail_cuda(e, "reduce launch");
+}
+
+constexpr int64_t kHostChunkKeys = int64_t{1} << 24;  // 64 MiB of keys per staged chunk
+
+int run_host(const int32_t* h_keys, int64_t n, int32_t num_bins, uint32_t* h_bins,
+             cudaStream_t stream) {
+  int rc = check_args(h_keys, n, num_bins, h_bins);
+  if (rc) return rc;
+  DeviceState* st = nullptr;
+  dsmem_hist_plan_t plan;
+  const int64_t chunk = n < kHostChunkKeys ? n : kHostChunkKeys;
+  {
+    std::lock_guard<std::mutex> g(g_mutex);
+    if ((rc = device_state(&st))) return rc;
+    if ((rc = plan_locked(st, num_bins, chunk, nullptr, &plan))) return rc;
+    if ((rc = ensure_pool(st))) return rc;
+    cudaError_t e;
+    if (!st->copy_stream) {
+      if ((e = cudaStreamCreateWithFlags(&st->copy_stream, cudaStreamNonBlocking)) != cudaSuccess)
+        return fail_cuda(e, "cudaStreamCreateWithFlags");
+      for (int i = 0; i < 2; ++i) {
+        if ((e = cudaEventCreateWithFlags(&st->ev_copied[i], cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&st->ev_consumed[i], cudaEventDisableTiming)) != cudaSuccess)
+          return fail_cuda(e, "cudaEventCreateWithFlags");
+      }
+    }
+  }
+  std::lock_guard<std::mutex> serial(st->host_call);
+  cudaError_t e;
+  const size_t bins_bytes = sizeof(uint32_t) * static_cast<size_t>(num_bins);
+  const size_t bins_alloc = (bins_bytes + 255) & ~size_t{255};
+  const size_t chunk_bytes = ((sizeof(int32_t) * static_cast<size_t>(chunk)) + 255) & ~size_t{255};
+  const size_t total = bins_alloc + static_cast<size_t>(plan.workspace_bytes) + 2 * chunk_bytes;
+  void* scratch = nullptr;
+  if ((e = cudaMallocFromPoolAsync(&scratch, total, st->pool, stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(DSMEM_HIST_ENOMEM, "scratch pool: %zu bytes: %s", total, cudaGetErrorString(e));
+  }
+  char* base = static_cast<char*>(scratch);
+  uint32_t* d_bins = reinterpret_cast<uint32_t*>(base);
+  uint32_t* partials = reinterpret_cast<uint32_t*>(base + bins_alloc);
+  int32_t* stage[2] = {
+      reinterpret_cast<int32_t*>(base + bins_alloc + plan.workspace_bytes),
+      reinterpret_cast<int32_t*>(base + bins_alloc + plan.workspace_bytes + chunk_bytes)};
+
+  // Order the copy stream after the allocation made on `stream`.
+  rc = DSMEM_HIST_OK;
+  if ((e = cudaEventRecord(st->ev_consumed[0], stream)) != cudaSuccess ||
+      (e = cudaEventRecord(st->ev_consumed[1], stream)) != cudaSuccess)
+    rc = fail_cuda(e, "cudaEventRecord");
+  if (n == 0 && rc == DSMEM_HIST_OK) {
+    if ((e = cudaMemsetAsync(d_bins, 0, bins_bytes, stream)) != cudaSuccess)
+      rc = fail_cuda(e, "cudaMemsetAsync");
+  }
+  for (int64_t off = 0, j = 0; rc == DSMEM_HIST_OK && off < n; off += chunk, ++j) {
+    const int b = static_cast<int>(j & 1);
+    const int64_t cnt = (n - off) < chunk ? (n - off) : chunk;
+    if ((e = cudaStreamWaitEvent(st->copy_stream, st->ev_consumed[b], 0)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(stage[b], h_keys + off, sizeof(int32_t) * cnt,
+                             cudaMemcpyHostToDevice, st->copy_stream)) != cudaSuccess ||
+        (e = cudaEventRecord(st->ev_copied[b], st->copy_stream)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(stream, st->ev_copied[b], 0)) != cudaSuccess) {
+      rc = fail_cuda(e, "staging copy");
+      break;
+    }
+    const ClusterHistArgs args = make_args(plan, stage[b], cnt, num_bins, partials, j > 0);
+    if ((e = launch_cluster_hist(plan, args, stream)) != cudaSuccess ||
+        (e = cudaEventRecord(st->ev_consumed[b], stream)) != cudaSuccess) {
+      rc = fail_cuda(e, "cluster histogram launch");
+      break;
+    }
+  }
+  if (rc == DSMEM_HIST_OK && n > 0) {
+    if ((e = launch_reduce_partials(partials, static_cast<uint64_t>(plan.partial_stride),
+                                    static_cast<uint32_t>(plan.num_clusters),
+                                    static_cast<uint32_t>(num_bins), d_bins, stream)) != cudaSuccess)
+      rc = fail_cuda(e, "reduce launch");
+  }
+  if (rc == DSMEM_HIST_OK) {
+    if ((e = cudaMemcpyAsync(h_bins, d_bins, bins_bytes, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+      rc = fail_cuda(e, "result copy");
+  }
+  // The copy stream's last use of the staging buffers is ordered before the
+  // kernels on `stream`, so freeing on `stream` is safe.
+  cudaFreeAsync(scratch, stream);
+  if ((e = cudaStreamSynchronize(stream)) != cudaSuccess && rc == DSMEM_HIST_OK)
+    rc = fail_cuda(e, "cudaStreamSynchronize");
+  return rc;
+}
+
+}  // namespace
+}  // namespace dsmh
+
+using namespace dsmh;
+
+extern "C" {
+
+int dsmem_hist(const int32_t* keys, int64_t n, int32_t num_bins, uint32_t* bins,
+               cudaStream_t stream) {
+  return run_device(keys, n, num_bins, bins, nullptr, stream);
+}
+
+int dsmem_hist_ex(const int32_t* keys, int64_t n, int32_t num_bins, uint32_t* bins,
+                  const dsmem_hist_request_t* request, cudaStream_t stream) {
+  return run_device(keys, n, num_bins, bins, request, stream);
+}
+
+int dsmem_hist_global_atomic(const int32_t* keys, int64_t n, int32_t num_bins, uint32_t* bins,
+                             cudaStream_t stream) {
+  int rc = check_args(keys, n, num_bins, bins);
+  if (rc) return rc;
+  const cudaError_t e = launch_global_atomic(keys, n, static_cast<uint32_t>(num_bins), bins, stream);
+  return e == cudaSuccess ? DSMEM_HIST_OK : fail_cuda(e, "global-atomic histogram launch");
+}
+
+int dsmem_hist_host(const int32_t* h_keys, int64_t n, int32_t num_bins, uint32_t* h_bins,
+                    cudaStream_t stream) {
+  return run_host(h_keys, n, num_bins, h_bins, stream);
+}
+
+int dsmem_hist_partials(const int32_t* keys, int64_t n, int32_t num_bins,
+                        const dsmem_hist_plan_t* plan, uint32_t* partials, int32_t accumulate,
+                        cudaStream_t stream) {
+  return run_partials(keys, n, num_bins, plan, partials, accumulate, stream);
+}
+
+int dsmem_hist_reduce(const uint32_t* partials, int32_t num_clusters, int64_t partial_stride,
+                      int32_t num_bins, uint32_t* bins, cudaStream_t stream) {
+  return run_reduce(partials, num_clusters, partial_stride, num_bins, bins, stream);
+}
+
+int dsmem_hist_plan(int32_t num_bins, int64_t n, const dsmem_hist_request_t* request,
+                    dsmem_hist_plan_t* out) {
+  if (!out) return fail(DSMEM_HIST_EINVAL, "out is NULL");
+  std::lock_guard<std::mutex> g(g_mutex);
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  return plan_locked(st, num_bins, n, request, out);
+}
+
+int dsmem_hist_plan_for_device(const dsmem_hist_device_t* device, int32_t num_bins, int64_t n,
+                               const dsmem_hist_request_t* request, int32_t max_active_clusters,
+                               dsmem_hist_plan_t* out) {
+  const char* why = "";
+  const int rc = plan_shape(device, num_bins, n, request, max_active_clusters, out, &why);
+  return rc == DSMEM_HIST_OK ? rc : fail(rc, "plan: %s", why);
+}
+
+const char* dsmem_hist_strerror(int code) {
+  switch (code) {
+    case DSMEM_HIST_OK: return "DSMEM_HIST_OK";
+    case DSMEM_HIST_EINVAL: return "DSMEM_HIST_EINVAL: invalid argument";
+    case DSMEM_HIST_EUNSUPPORTED: return "DSMEM_HIST_EUNSUPPORTED: unsupported device or shape";
+    case DSMEM_HIST_ECUDA: return "DSMEM_HIST_ECUDA: CUDA runtime error";
+    case DSMEM_HIST_ETIMEOUT: return "DSMEM_HIST_ETIMEOUT: device-side wait timed out";
+    case DSMEM_HIST_ENOMEM: return "DSMEM_HIST_ENOMEM: scratch allocation failed";
+    default: return "DSMEM_HIST: unknown error code";
+  }
+}
+
+const char* dsmem_hist_last_error(void) { return g_last_error.c_str(); }
+
+void dsmem_hist_release(void) {
+  std::lock_guard<std::mutex> g(g_mutex);
+  int cur = 0;
+  const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
+  for (auto& kv : g_devices) {
+    DeviceState* st = kv.second;
+    if (!st) continue;
+    if (cudaSetDevice(kv.first) != cudaSuccess) continue;
+    if (st->pool) {
+      cudaDeviceSynchronize();
+      cudaMemPoolDestroy(st->pool);
+      st->pool = nullptr;
+    }
+    if (st->copy_stream) {
+      cudaStreamDestroy(st->copy_stream);
+      st->copy_stream = nullptr;
+      for (int i = 0; i < 2; ++i) {
+        cudaEventDestroy(st->ev_copied[i]);
+        cudaEventDestroy(st->ev_consumed[i]);
+        st->ev_copied[i] = st->ev_consumed[i] = nullptr;
+      }
+    }
+  }
+  if (have_cur) cudaSetDevice(cur);
+}
+
+int dsmem_hist_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,63 @@
+// Internal interfaces between the kernel translation unit and the host layer
+// of libdsmemhist.  Not installed; the public C ABI is include/dsmem_hist.h.
+#pragma once
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#include "dsmem_hist.h"
+
+namespace dsmh {
+
+// Keys every thread handles per unrolled step of the streaming loop: four
+// 16-byte vectors of four int32 keys.
+constexpr int kVecPerThread = 4;
+constexpr int kKeysPerThreadStep = 4 * kVecPerThread;
+// The planner gives every CTA at least this many unrolled steps of work.
+constexpr int kMinStepsPerCta = 4;
+// Default cap on one CTA's counter slice: 128 KiB leaves room for a second
+// small allocation per SM while keeping the slice count at the published
+// cluster sizes (2 x 32768 bins, 8 x 32768, 16 x 32768).
+constexpr int kDefaultSliceCapBytes = 128 * 1024;
+// Scratch bound the planner keeps the partial rows under when it picks C.
+constexpr int64_t kMaxAutoScratchBytes = int64_t{1} << 30;
+// Shared memory the runtime reserves per CTA on sm_90 and later.
+constexpr int kSmemReservedPerCta = 1024;
+
+// Arguments of one cluster-histogram launch (passed by value).
+struct ClusterHistArgs {
+  const int32_t* keys;
+  int64_t n;
+  uint32_t* partials;   // [num_clusters][stride] u32, one row per cluster
+  uint32_t num_bins;
+  uint32_t S;           // counters per CTA slice (multiple of 4)
+  uint64_t magic;       // floor(2^40 / S) + 1: owner = (rel * magic) >> 40
+  uint32_t passes;      // bin ranges of P*S bins
+  uint64_t stride;      // partial row stride (u32 elements, multiple of 4)
+  uint32_t head;        // keys before the first 16-byte boundary of `keys` (0..3, <= n)
+  uint32_t accumulate;  // 1: add the slice into the partial row, 0: overwrite it
+};
+
+// Launches (all asynchronous on `stream`).
+cudaError_t launch_cluster_hist(const dsmem_hist_plan_t& plan, const ClusterHistArgs& args,
+                                cudaStream_t stream);
+cudaError_t launch_reduce_partials(const uint32_t* partials, uint64_t stride,
+                                   uint32_t num_clusters, uint32_t num_bins, uint32_t* bins,
+                                   cudaStream_t stream);
+cudaError_t launch_global_atomic(const int32_t* keys, int64_t n, uint32_t num_bins,
+                                 uint32_t* bins, cudaStream_t stream);
+
+// Sets the kernel attributes a shape needs (dynamic shared memory above
+// 48 KiB, non-portable cluster sizes) on the current device.
+cudaError_t prepare_cluster_kernel(int aggregate, int smem_bytes);
+// Occupancy query: clusters of this shape that can be resident at once.
+cudaError_t query_max_active_clusters(int aggregate, int cluster_size, int block_threads,
+                                      int smem_bytes, int* out);
+
+// Planner (pure host logic, planner.cpp).
+int plan_shape(const dsmem_hist_device_t* dev, int32_t num_bins, int64_t n,
+               const dsmem_hist_request_t* req, int32_t max_active_clusters,
+               dsmem_hist_plan_t* out, const char** why);
+uint64_t owner_magic(uint32_t S);
+
+}  // namespace dsmh

@@ -1,0 +1,186 @@
+/*
+ * dsmem_hist -- thread-block-cluster histogram for NVIDIA GB300 (sm_103a).
+ *
+ * The operation ("Distributed Shared Memory", section "The cluster
+ * histogram"): a bin array too large for one CTA's shared memory is split
+ * into equal slices of S counters, one slice in the shared memory of each of
+ * the P CTAs of a thread-block cluster (owner = bin / S).  Every thread
+ * increments the owning CTA's counter through distributed shared memory,
+ * cluster barriers bracket that phase, and the per-cluster slices are then
+ * reduced into global memory.  The result is the plain histogram:
+ *
+ *     bins[b] = #{ i in [0, n) : keys[i] == b }  (mod 2^32),  0 <= b < num_bins
+ *
+ * Conventions for every entry point:
+ *   - Return value: 0 (DSMEM_HIST_OK) or one of the negative codes below;
+ *     dsmem_hist_strerror() names a code and dsmem_hist_last_error() gives
+ *     the calling thread's most recent detailed message (CUDA error text
+ *     included).
+ *   - Keys are int32; keys outside [0, num_bins) -- negatives included --
+ *     are not counted.  `bins` is OVERWRITTEN (not accumulated into).
+ *   - Counters are uint32 and wrap modulo 2^32.
+ *   - Device pointers belong to the caller and must be valid on the current
+ *     CUDA device; `keys` must be 4-byte aligned (any 16-byte misalignment is
+ *     handled), `bins` 4-byte aligned.
+ *   - Device entry points are asynchronous on `stream` (0 = legacy default
+ *     stream): they return after enqueueing, results are valid once the
+ *     stream has reached that point.  Scratch memory (per-cluster partial
+ *     histograms) comes from a library-owned, stream-ordered CUDA memory pool
+ *     and is returned to the pool on the same stream, so calls on different
+ *     streams never share scratch.
+ *   - Thread-safe: the per-device state is guarded by a mutex.
+ */
+#ifndef DSMEM_HIST_H
+#define DSMEM_HIST_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define DSMEM_HIST_API __attribute__((visibility("default")))
+#else
+#define DSMEM_HIST_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  DSMEM_HIST_OK = 0,
+  DSMEM_HIST_EINVAL = -1,       /* bad argument (null pointer with n > 0, n < 0, num_bins < 1, misaligned) */
+  DSMEM_HIST_EUNSUPPORTED = -2, /* device below compute capability 9.0, or no legal cluster shape */
+  DSMEM_HIST_ECUDA = -3,        /* a CUDA runtime call or kernel launch failed */
+  DSMEM_HIST_ETIMEOUT = -4,     /* a bounded device-side wait gave up (reported by a later sync) */
+  DSMEM_HIST_ENOMEM = -5        /* the scratch pool could not supply the partial histograms */
+};
+
+/* Launch shape chosen by the planner (all fields filled by dsmem_hist_plan*). */
+typedef struct dsmem_hist_plan {
+  int32_t cluster_size;        /* P: CTAs per cluster, 1..16 (16 is non-portable) */
+  int32_t bins_per_cta;        /* S: counters in each CTA's shared-memory slice (multiple of 4) */
+  int32_t passes;              /* bin ranges of P*S bins streamed one after the other (1 unless
+                                  num_bins exceeds what one cluster holds) */
+  int32_t block_threads;       /* threads per CTA */
+  int32_t num_clusters;        /* C: clusters launched (persistent grid of C*P CTAs) */
+  int32_t smem_bytes;          /* dynamic shared memory per CTA: 4*S */
+  int32_t aggregate;           /* 1: warp pre-aggregation of equal keys (__match_any_sync + popc) */
+  int32_t ctas_per_sm;         /* resident CTAs per SM the shape allows */
+  int32_t max_active_clusters; /* occupancy answer for this shape (0 when not queried) */
+  int32_t reserved;            /* zero */
+  int64_t partial_stride;      /* u32 elements between two clusters' partial rows (num_bins rounded up to 4) */
+  int64_t workspace_bytes;     /* scratch: num_clusters * partial_stride * 4 */
+} dsmem_hist_plan_t;
+
+/* Planner overrides; a zero field (or -1 for `aggregate`) means "choose". */
+typedef struct dsmem_hist_request {
+  int32_t cluster_size;    /* force P (1..16) */
+  int32_t block_threads;   /* force threads per CTA (multiple of 32, 64..1024) */
+  int32_t num_clusters;    /* force C */
+  int32_t aggregate;       /* -1 choose, 0 off, 1 on */
+  int32_t max_slice_bytes; /* cap on 4*S (default 128 KiB) */
+} dsmem_hist_request_t;
+
+/* The device facts the planner uses; filled from cudaGetDeviceProperties by
+ * dsmem_hist_plan, or by hand to plan for a described device. */
+typedef struct dsmem_hist_device {
+  int32_t cc_major, cc_minor;
+  int32_t sm_count;
+  int32_t max_smem_per_block_optin; /* bytes a CTA may opt in to */
+  int32_t max_smem_per_sm;          /* bytes per SM */
+  int32_t max_threads_per_sm;
+  int32_t max_cluster_size;         /* 8 portable, 16 where non-portable sizes are allowed */
+} dsmem_hist_device_t;
+
+/* Histogram of n int32 keys into num_bins uint32 counters on the GPU, through
+ * the cluster/DSMEM path with the planner's shape ("Distributed Shared
+ * Memory", section "The cluster histogram").
+ *   keys     device, n int32 keys (read only)
+ *   n        >= 0; n == 0 zeroes `bins`
+ *   num_bins >= 1; more bins than one cluster holds are streamed in passes
+ *   bins     device, num_bins uint32 (overwritten)
+ *   stream   CUDA stream the work is enqueued on
+ * Errors: EINVAL for bad arguments (nothing enqueued), EUNSUPPORTED, ECUDA,
+ * ENOMEM. */
+DSMEM_HIST_API int dsmem_hist(const int32_t* keys, int64_t n, int32_t num_bins, uint32_t* bins,
+               cudaStream_t stream);
+
+/* Same as dsmem_hist with planner overrides (NULL = none).  Used to force a
+ * cluster size, block size, grid or aggregation mode; the forced shape must
+ * be legal on the device or EUNSUPPORTED is returned. */
+DSMEM_HIST_API int dsmem_hist_ex(const int32_t* keys, int64_t n, int32_t num_bins, uint32_t* bins,
+                  const dsmem_hist_request_t* request, cudaStream_t stream);
+
+/* Comparison point ("Distributed Shared Memory", section "When it beats global
+ * atomics"): zero `bins`, then one global atomic add per in-range key,
+ * contended grid-wide.  Same arguments, semantics and errors as dsmem_hist;
+ * uses no scratch. */
+DSMEM_HIST_API int dsmem_hist_global_atomic(const int32_t* keys, int64_t n, int32_t num_bins, uint32_t* bins,
+                             cudaStream_t stream);
+
+/* Histogram of HOST keys into HOST bins: the keys are copied to the device in
+ * chunks on an internal copy stream, overlapped with the cluster kernel on
+ * `stream`, and the bins copied back.  Pinned host memory gives full copy
+ * speed; pageable memory works but copies slower.  SYNCHRONOUS: returns after
+ * `h_bins` holds the result.  Device scratch (two chunk buffers, partial
+ * histograms, the device bins) comes from the library's stream-ordered pool. */
+DSMEM_HIST_API int dsmem_hist_host(const int32_t* h_keys, int64_t n, int32_t num_bins, uint32_t* h_bins,
+                    cudaStream_t stream);
+
+/* Stage 1 of dsmem_hist, with caller-owned scratch: every cluster of `plan`
+ * writes (accumulate == 0) or adds into (accumulate == 1) its partial row
+ *     partials[c * plan->partial_stride + b],  c < plan->num_clusters,
+ * which, summed over c, is the histogram of these keys ("Distributed Shared
+ * Memory", section "The cluster histogram": zero, barrier, DSMEM increments,
+ * barrier, flush).
+ *   plan      from dsmem_hist_plan for the same num_bins (checked for
+ *             consistency; EINVAL otherwise)
+ *   partials  device, 16-byte aligned, num_clusters * partial_stride uint32;
+ *             with accumulate == 1 it must hold the rows of an earlier call
+ *             with the same plan (used to fold key chunks into one histogram)
+ * Asynchronous on `stream`. */
+DSMEM_HIST_API int dsmem_hist_partials(const int32_t* keys, int64_t n, int32_t num_bins,
+                                       const dsmem_hist_plan_t* plan, uint32_t* partials,
+                                       int32_t accumulate, cudaStream_t stream);
+
+/* Stage 2 of dsmem_hist: bins[b] = sum over c < num_clusters of
+ * partials[c * partial_stride + b] (mod 2^32), b < num_bins.
+ *   partials  device, 16-byte aligned; partial_stride a multiple of 4 and
+ *             >= num_bins
+ *   bins      device, num_bins uint32 (overwritten)
+ * Asynchronous on `stream`. */
+DSMEM_HIST_API int dsmem_hist_reduce(const uint32_t* partials, int32_t num_clusters,
+                                     int64_t partial_stride, int32_t num_bins, uint32_t* bins,
+                                     cudaStream_t stream);
+
+/* Plan for the current device (queries its properties and the occupancy of
+ * the chosen shape).  `request` may be NULL. */
+DSMEM_HIST_API int dsmem_hist_plan(int32_t num_bins, int64_t n, const dsmem_hist_request_t* request,
+                    dsmem_hist_plan_t* out);
+
+/* Plan for a described device without touching CUDA (host logic only).
+ * `max_active_clusters` is the occupancy answer to use for the chosen shape;
+ * pass 0 to estimate it as floor(sm_count * ctas_per_sm / P). */
+DSMEM_HIST_API int dsmem_hist_plan_for_device(const dsmem_hist_device_t* device, int32_t num_bins, int64_t n,
+                               const dsmem_hist_request_t* request, int32_t max_active_clusters,
+                               dsmem_hist_plan_t* out);
+
+/* Name of an error code (static string). */
+DSMEM_HIST_API const char* dsmem_hist_strerror(int code);
+
+/* The calling thread's most recent error message ("" if none). */
+DSMEM_HIST_API const char* dsmem_hist_last_error(void);
+
+/* Frees the library's cached device resources (memory pools, copy streams,
+ * events) on every device it touched.  Call only when no dsmem_hist work is
+ * in flight; later calls recreate what they need. */
+DSMEM_HIST_API void dsmem_hist_release(void);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+DSMEM_HIST_API int dsmem_hist_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSMEM_HIST_H */

@@ -1,0 +1,157 @@
+"""The C ABI without a GPU: the library loads, exports every declared entry
+point, rejects bad arguments before touching CUDA, and plans shapes for a
+described device (host logic only)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import cluster_distributed_shared_gb300 as pkg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+GB300 = dict(cc_major=10, cc_minor=3, sm_count=152, max_smem_per_block_optin=232448,
+             max_smem_per_sm=233472, max_threads_per_sm=2048, max_cluster_size=16)
+H100 = dict(cc_major=9, cc_minor=0, sm_count=132, max_smem_per_block_optin=232448,
+            max_smem_per_sm=233472, max_threads_per_sm=2048, max_cluster_size=16)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def declared_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            names += re.findall(r"^DSMEM_HIST_API\s+[\w\s\*]*?\b(\w+)\s*\(", text, re.M)
+    return names
+
+
+def test_library_exports_every_declared_symbol():
+    names = declared_functions()
+    assert "dsmem_hist" in names and len(names) >= 10
+    L = pkg.lib()
+    for name in names:
+        assert hasattr(L, name), name
+    assert set(pkg.EXPORTS) <= set(names)
+
+
+def test_version_and_strerror():
+    assert pkg.dsmem_hist_version() >= 100
+    for code in (0, -1, -2, -3, -4, -5):
+        assert pkg.strerror(code).startswith("DSMEM_HIST")
+
+
+@pytest.mark.parametrize("fn", ["dsmem_hist", "dsmem_hist_global_atomic", "dsmem_hist_host"])
+def test_invalid_arguments_rejected_before_cuda(fn):
+    L = pkg.lib()
+    f = getattr(L, fn)
+    buf = (ctypes.c_uint32 * 8)()
+    p = ctypes.cast(buf, ctypes.c_void_p)
+    cases = [
+        (p, -1, 8, p),              # n < 0
+        (p, 4, 0, p),               # num_bins < 1
+        (p, 4, -5, p),              # num_bins < 1
+        (None, 4, 8, p),            # keys NULL with n > 0
+        (p, 4, 8, None),            # bins NULL
+        (ctypes.c_void_p(ctypes.addressof(buf) + 2), 1, 8, p),  # misaligned keys
+        (p, 1, 8, ctypes.c_void_p(ctypes.addressof(buf) + 1)),  # misaligned bins
+    ]
+    for keys, n, nb, bins in cases:
+        assert f(keys, n, nb, bins, None) == pkg.DSMEM_HIST_EINVAL
+        assert L.dsmem_hist_last_error()
+
+
+def plan(dev, nb, n, mac=0, **kw):
+    return pkg.dsmem_hist_plan_for_device(dev, nb, n, mac, **kw)
+
+
+@pytest.mark.parametrize("nb,n,P,S", [
+    (8192, 1 << 20, 2, 4096),
+    (65536, 1 << 26, 2, 32768),
+    (262144, 1 << 28, 8, 32768),
+    (524288, 1 << 30, 16, 32768),
+])
+def test_planner_matches_published_cluster_shapes(nb, n, P, S):
+    p = plan(GB300, nb, n, cluster_size=P)
+    assert (p["cluster_size"], p["bins_per_cta"], p["passes"]) == (P, S, 1)
+    assert p["smem_bytes"] == 4 * S
+    q = plan(GB300, nb, n)          # the planner's own choice agrees here
+    assert (q["cluster_size"], q["bins_per_cta"]) == (P, S)
+
+
+@pytest.mark.parametrize("nb", [1, 2, 3, 5, 97, 4095, 4096, 4097, 65535, 65537, 100003, 262143,
+                                524289, 929792, 929793, 1 << 22, 2**31 - 1])
+@pytest.mark.parametrize("slice_cap", [0, 1024, 232448])
+def test_planner_covers_every_bin(nb, slice_cap):
+    for forced in (0, 1, 2, 16):
+        p = plan(GB300, nb, 1 << 20, cluster_size=forced, max_slice_bytes=slice_cap)
+        P, S, passes = p["cluster_size"], p["bins_per_cta"], p["passes"]
+        assert S % 4 == 0 and S >= 4
+        cap = (slice_cap or 128 * 1024)
+        assert 4 * S <= min(cap, GB300["max_smem_per_block_optin"]) or 4 * S == 16
+        assert passes * P * S >= nb                       # no bin dropped
+        assert (passes - 1) * P * S < nb                  # no empty pass
+        assert P * S < 2 ** 20 + 16 * 4                    # owner arithmetic range
+        assert p["partial_stride"] % 4 == 0 and p["partial_stride"] >= nb
+        assert p["workspace_bytes"] == p["num_clusters"] * p["partial_stride"] * 4
+        if forced:
+            assert P == forced
+
+
+def test_owner_magic_exact():
+    # owner = (rel * (floor(2^40 / S) + 1)) >> 40 must equal rel // S for every
+    # rel < P * S the kernel can see (checked exhaustively at the slice sizes'
+    # extremes, and on a grid in between).
+    for S in [4, 8, 12, 4096, 25004, 32768, 58108, 58112]:
+        magic = (1 << 40) // S + 1
+        P = 16
+        rels = list(range(0, min(P * S, 200000))) + list(range(max(0, P * S - 200000), P * S))
+        for rel in rels[:: max(1, len(rels) // 50000)] + [P * S - 1]:
+            assert (rel * magic) >> 40 == rel // S, (S, rel)
+
+
+def test_planner_grid_and_threads():
+    p = plan(GB300, 262144, 1 << 28, mac=16)
+    assert p["num_clusters"] == 16 and p["block_threads"] == 1024 and p["ctas_per_sm"] == 1
+    small = plan(GB300, 8192, 1000, mac=100)
+    assert small["num_clusters"] == 1 and small["block_threads"] == 512
+    forced = plan(GB300, 8192, 1 << 20, mac=100, num_clusters=7, block_threads=256)
+    assert forced["num_clusters"] == 7 and forced["block_threads"] == 256
+
+
+def test_planner_multi_pass_when_bins_exceed_cluster():
+    p = plan(GB300, 1 << 22, 1 << 24)
+    assert p["cluster_size"] == 16 and p["passes"] == 8 and p["bins_per_cta"] == 32768
+    p8 = dict(GB300, max_cluster_size=8)
+    q = plan(p8, 524288, 1 << 24)
+    assert q["cluster_size"] == 8 and q["passes"] == 2
+
+
+def test_planner_errors():
+    old = dict(H100, cc_major=8)
+    with pytest.raises(pkg.DsmemHistError) as e:
+        plan(old, 1024, 10)
+    assert e.value.code == pkg.DSMEM_HIST_EUNSUPPORTED
+    with pytest.raises(pkg.DsmemHistError) as e:
+        plan(dict(GB300, max_cluster_size=8), 1024, 10, cluster_size=16)
+    assert e.value.code == pkg.DSMEM_HIST_EUNSUPPORTED
+    for bad in [dict(cluster_size=17), dict(block_threads=100), dict(block_threads=2048),
+                dict(num_clusters=-1)]:
+        with pytest.raises(pkg.DsmemHistError) as e:
+            plan(GB300, 1024, 10, **bad)
+        assert e.value.code == pkg.DSMEM_HIST_EINVAL
+    with pytest.raises(pkg.DsmemHistError):
+        plan(GB300, 0, 10)
+
+
+def test_aggregate_override():
+    assert plan(GB300, 4096, 1 << 20, aggregate=0)["aggregate"] == 0
+    assert plan(GB300, 4096, 1 << 20, aggregate=1)["aggregate"] == 1

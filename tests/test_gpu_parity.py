@@ -1,0 +1,254 @@
+"""GPU parity: the CUDA library, called through its C ABI, against the CPU
+oracle, bit for bit (integer counts: one correct answer).
+
+Covers the pins, forced launch shapes (every cluster size, both aggregation
+modes, block sizes, misaligned key pointers, ragged lengths), multi-pass bin
+ranges, the five synthetic workloads at full size in the launch
+configuration the benchmark times, the global-atomics comparison kernel, the
+host-buffer entry point and concurrent streams.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import cluster_distributed_shared_gb300 as pkg  # noqa: E402
+import gen  # noqa: E402
+import oracle  # noqa: E402
+from tests import pins  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+# Cluster size each synthetic workload is published with.
+WORKLOAD_CLUSTER = {
+    "uniform-1M-8K": 2,
+    "uniform-64M-64K": 2,
+    "uniform-256M-256K": 8,
+    "zipf1.1-256M-256K": 8,
+    "runs256-1G-512K": 16,
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda_ready():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.init()
+    yield
+    torch.cuda.synchronize()
+
+
+def to_np(t):
+    return t.cpu().numpy().view(np.uint32)
+
+
+def gpu_hist(keys, num_bins, out=None, **kw):
+    d = torch.from_numpy(np.ascontiguousarray(keys, np.int32)).cuda()
+    o = None
+    if out is not None:
+        o = torch.from_numpy(out.view(np.int32)).cuda()
+    r = pkg.dsmem_hist(d, num_bins, out=o, **kw)
+    torch.cuda.synchronize()
+    return to_np(r)
+
+
+def forced(**kw):
+    return lambda keys, num_bins, out=None: gpu_hist(keys, num_bins, out, **kw)
+
+
+def global_atomic(keys, num_bins, out=None):
+    d = torch.from_numpy(np.ascontiguousarray(keys, np.int32)).cuda()
+    o = None if out is None else torch.from_numpy(out.view(np.int32)).cuda()
+    r = pkg.dsmem_hist_global_atomic(d, num_bins, out=o)
+    torch.cuda.synchronize()
+    return to_np(r)
+
+
+@pytest.mark.parametrize("pin", pins.ALL_PINS, ids=lambda p: p.__name__)
+def test_pins_default_plan(pin):
+    pin(gpu_hist)
+
+
+@pytest.mark.parametrize("shape", [
+    dict(cluster_size=1, aggregate=0), dict(cluster_size=2, aggregate=1),
+    dict(cluster_size=4, aggregate=0, block_threads=256), dict(cluster_size=8, aggregate=1),
+    dict(cluster_size=16, aggregate=0), dict(cluster_size=16, aggregate=1, block_threads=64),
+], ids=str)
+@pytest.mark.parametrize("pin", [pins.pin_brute_force_tiny, pins.pin_cycle,
+                                 pins.pin_constructed_counts, pins.pin_single_value,
+                                 pins.pin_out_of_range, pins.pin_overwrite, pins.pin_empty],
+                         ids=lambda p: p.__name__)
+def test_pins_forced_shapes(pin, shape):
+    pin(forced(**shape))
+
+
+@pytest.mark.parametrize("pin", [pins.pin_brute_force_tiny, pins.pin_cycle,
+                                 pins.pin_single_value, pins.pin_out_of_range,
+                                 pins.pin_overwrite, pins.pin_empty], ids=lambda p: p.__name__)
+def test_pins_global_atomic(pin):
+    pin(global_atomic)
+
+
+@pytest.mark.parametrize("num_bins", [8192, 65536, 100003, 262144, 524288])
+def test_forced_shape_sweep(num_bins):
+    n = 5_000_003
+    base = gen.uniform(n + 3, num_bins + num_bins // 16, seed=num_bins)  # ~6% out of range
+    base[::1001] = -7
+    dev = torch.from_numpy(base).cuda()
+    for off in (0, 3):
+        keys_np = base[off:off + n]
+        want = oracle.histogram(keys_np, num_bins)
+        keys = dev[off:off + n]
+        for P in (1, 2, 4, 8, 16):
+            for agg in (0, 1):
+                for threads in (256, 1024):
+                    got = pkg.dsmem_hist(keys, num_bins, cluster_size=P, aggregate=agg,
+                                         block_threads=threads)
+                    torch.cuda.synchronize()
+                    g = to_np(got)
+                    assert np.array_equal(g, want), (num_bins, off, P, agg, threads,
+                                                     np.flatnonzero(g != want)[:8])
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 31, 32, 33, 127, 128, 129, 130, 511, 4099, 65537])
+def test_ragged_small_lengths(n):
+    num_bins = 37
+    base = gen.uniform(n + 3, 40, seed=n)
+    dev = torch.from_numpy(base).cuda()
+    for off in (0, 1, 2, 3):
+        want = oracle.histogram(base[off:off + n], num_bins)
+        for agg in (0, 1):
+            got = pkg.dsmem_hist(dev[off:off + n], num_bins, cluster_size=2, aggregate=agg,
+                                 num_clusters=3)
+            torch.cuda.synchronize()
+            assert np.array_equal(to_np(got), want), (n, off, agg)
+
+
+def test_multi_pass_bin_ranges():
+    n = 3_000_001
+    for num_bins, kw in [(1 << 22, {}), (100003, dict(max_slice_bytes=4096)),
+                         (929792, dict(max_slice_bytes=232448, cluster_size=16)),
+                         (1 << 21, dict(cluster_size=2, aggregate=0))]:
+        keys = gen.uniform(n, num_bins, seed=num_bins)
+        plan = pkg.dsmem_hist_plan(num_bins, n, **kw)
+        got = gpu_hist(keys, num_bins, **kw)
+        assert np.array_equal(got, oracle.histogram(keys, num_bins)), (num_bins, plan)
+    assert pkg.dsmem_hist_plan(1 << 22, n)["passes"] > 1
+
+
+def test_max_slice_single_pass():
+    # Largest slice a CTA can opt in to, with the largest cluster.
+    plan = pkg.dsmem_hist_plan(929792, 1 << 24, cluster_size=16, max_slice_bytes=232448)
+    assert plan["passes"] == 1 and plan["smem_bytes"] == 232448
+    keys = gen.uniform(1 << 24, 1 << 20, seed=4)
+    got = gpu_hist(keys, 929792, cluster_size=16, max_slice_bytes=232448)
+    assert np.array_equal(got, oracle.histogram(keys, 929792))
+
+
+def _full_workload(name, seed):
+    keys = gen.workload(name, seed)
+    num_bins = gen.WORKLOADS[name]["num_bins"]
+    return keys, num_bins
+
+
+@pytest.mark.parametrize("name,seed", [(w, s) for w in WORKLOAD_CLUSTER for s in (0, 1, 2)] +
+                         [(w, s) for w in ("uniform-1M-8K", "uniform-64M-64K") for s in range(3, 10)])
+def test_workload_full_size(name, seed):
+    keys, num_bins = _full_workload(name, seed)
+    want = oracle.histogram(keys, num_bins)
+    assert int(want.sum(dtype=np.uint64)) == keys.size  # every generated key is in range
+    d = torch.from_numpy(keys).cuda()
+    del keys
+    P = WORKLOAD_CLUSTER[name]
+    plan = pkg.dsmem_hist_plan(num_bins, d.numel(), cluster_size=P)
+    assert plan["cluster_size"] == P and plan["bins_per_cta"] == num_bins // P
+    assert plan["passes"] == 1
+    out = torch.full((num_bins,), -1, dtype=torch.int32, device="cuda")
+    for kw in (dict(cluster_size=P), {}):   # the benchmark's shape, then the planner's
+        pkg.dsmem_hist(d, num_bins, out=out, **kw)
+        torch.cuda.synchronize()
+        got = to_np(out)
+        assert np.array_equal(got, want), (name, seed, kw, np.flatnonzero(got != want)[:8])
+    if seed == 0:
+        pkg.dsmem_hist_global_atomic(d, num_bins, out=out)
+        torch.cuda.synchronize()
+        assert np.array_equal(to_np(out), want)
+        pkg.dsmem_hist(d, num_bins, out=out, cluster_size=P, aggregate=1 - plan["aggregate"])
+        torch.cuda.synchronize()
+        assert np.array_equal(to_np(out), want)
+    del d
+    torch.cuda.empty_cache()
+
+
+def test_host_entry_point():
+    num_bins = 262144
+    for n in (0, 1, 4099, (1 << 24) + 12345, 3 * (1 << 24) + 7):
+        keys = gen.uniform(n, num_bins, seed=n)
+        want = oracle.histogram(keys, num_bins)
+        got = pkg.dsmem_hist_host(keys, num_bins)                 # pageable numpy
+        assert np.array_equal(got, want), n
+        pinned = torch.from_numpy(keys).pin_memory()
+        out = torch.empty(num_bins, dtype=torch.int32).pin_memory()
+        pkg.dsmem_hist_host(pinned, num_bins, out=out)             # pinned torch
+        assert np.array_equal(out.numpy().view(np.uint32), want), n
+
+
+def test_two_streams_do_not_share_scratch():
+    num_bins = 262144
+    a_np = gen.uniform(1 << 24, num_bins, seed=21)
+    b_np = gen.zipf(1 << 24, num_bins, seed=22)
+    want_a, want_b = oracle.histogram(a_np, num_bins), oracle.histogram(b_np, num_bins)
+    a, b = torch.from_numpy(a_np).cuda(), torch.from_numpy(b_np).cuda()
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    torch.cuda.synchronize()
+    for i in range(6):
+        with torch.cuda.stream(sa):
+            outs.append(("a", pkg.dsmem_hist(a, num_bins, stream=sa)))
+        with torch.cuda.stream(sb):
+            outs.append(("b", pkg.dsmem_hist(b, num_bins, stream=sb)))
+    torch.cuda.synchronize()
+    for tag, o in outs:
+        assert np.array_equal(to_np(o), want_a if tag == "a" else want_b)
+
+
+def test_repeat_is_deterministic_across_shapes():
+    num_bins = 65536
+    keys = gen.zipf(1 << 22, num_bins, seed=5)
+    want = oracle.histogram(keys, num_bins)
+    d = torch.from_numpy(keys).cuda()
+    for i in range(5):
+        for kw in (dict(cluster_size=2), dict(cluster_size=4, num_clusters=1),
+                   dict(cluster_size=8, num_clusters=64), dict(aggregate=0), dict(aggregate=1)):
+            got = pkg.dsmem_hist(d, num_bins, **kw)
+            torch.cuda.synchronize()
+            assert np.array_equal(to_np(got), want), kw
+
+
+def test_errors_on_device():
+    d = torch.zeros(16, dtype=torch.int32, device="cuda")
+    with pytest.raises(pkg.DsmemHistError) as e:
+        pkg.dsmem_hist(d, 100, cluster_size=17)
+    assert e.value.code == pkg.DSMEM_HIST_EINVAL
+    with pytest.raises(pkg.DsmemHistError):
+        pkg.dsmem_hist(d, 100, block_threads=48)
+    with pytest.raises(TypeError):
+        pkg.dsmem_hist(d.cpu(), 100)
+    # the library stays usable after rejected calls
+    got = pkg.dsmem_hist(d, 100)
+    torch.cuda.synchronize()
+    want = np.zeros(100, np.uint32)
+    want[0] = 16
+    assert np.array_equal(to_np(got), want)
+
+
+def test_plan_on_device_confirms_cluster_16():
+    p = pkg.dsmem_hist_plan(524288, 1 << 30)
+    assert p["cluster_size"] == 16 and p["max_active_clusters"] >= 1
+    p8 = pkg.dsmem_hist_plan(262144, 1 << 28)
+    assert p8["cluster_size"] == 8 and p8["max_active_clusters"] >= 1
+    assert p8["num_clusters"] == p8["max_active_clusters"]
