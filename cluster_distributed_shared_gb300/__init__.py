@@ -26,6 +26,9 @@ DSMEM_HIST_ECUDA = -3
 DSMEM_HIST_ETIMEOUT = -4
 DSMEM_HIST_ENOMEM = -5
 
+KERNEL_DIRECT = 0
+KERNEL_SHIP = 1
+
 
 class DsmemHistError(RuntimeError):
     def __init__(self, code: int, message: str):
@@ -44,6 +47,9 @@ class Plan(ctypes.Structure):
         ("aggregate", ctypes.c_int32),
         ("ctas_per_sm", ctypes.c_int32),
         ("max_active_clusters", ctypes.c_int32),
+        ("kernel", ctypes.c_int32),
+        ("keys_per_thread", ctypes.c_int32),
+        ("sub_vectors", ctypes.c_int32),
         ("reserved", ctypes.c_int32),
         ("partial_stride", ctypes.c_int64),
         ("workspace_bytes", ctypes.c_int64),
@@ -60,6 +66,7 @@ class Request(ctypes.Structure):
         ("num_clusters", ctypes.c_int32),
         ("aggregate", ctypes.c_int32),
         ("max_slice_bytes", ctypes.c_int32),
+        ("kernel", ctypes.c_int32),
     ]
 
 
@@ -134,8 +141,9 @@ def _check(code: int) -> None:
         raise DsmemHistError(code, msg)
 
 
-def _request(cluster_size=0, block_threads=0, num_clusters=0, aggregate=-1, max_slice_bytes=0):
-    return Request(cluster_size, block_threads, num_clusters, aggregate, max_slice_bytes)
+def _request(cluster_size=0, block_threads=0, num_clusters=0, aggregate=-1, max_slice_bytes=0,
+             kernel=-1):
+    return Request(cluster_size, block_threads, num_clusters, aggregate, max_slice_bytes, kernel)
 
 
 def _stream_handle(stream):
@@ -166,7 +174,7 @@ def _out_bins(keys, num_bins, out):
 
 
 def dsmem_hist(keys, num_bins: int, out=None, stream=None, *, cluster_size=0, block_threads=0,
-               num_clusters=0, aggregate=-1, max_slice_bytes=0):
+               num_clusters=0, aggregate=-1, max_slice_bytes=0, kernel=-1):
     """Histogram of a CUDA int32 tensor into `num_bins` 32-bit counters.
 
     Returns a torch.int32 tensor holding the uint32 counts bit for bit (use
@@ -179,9 +187,10 @@ def dsmem_hist(keys, num_bins: int, out=None, stream=None, *, cluster_size=0, bl
     out = _out_bins(keys, num_bins, out)
     with torch.cuda.device(keys.device):
         forced = (cluster_size, block_threads, num_clusters, max_slice_bytes) != (0, 0, 0, 0) \
-            or aggregate != -1
+            or aggregate != -1 or kernel != -1
         if forced:
-            req = _request(cluster_size, block_threads, num_clusters, aggregate, max_slice_bytes)
+            req = _request(cluster_size, block_threads, num_clusters, aggregate, max_slice_bytes,
+                           kernel)
             _check(lib().dsmem_hist_ex(keys.data_ptr(), keys.numel(), int(num_bins),
                                        out.data_ptr(), ctypes.byref(req), _stream_handle(stream)))
         else:

@@ -44,9 +44,12 @@ struct DeviceState {
   cudaStream_t copy_stream = nullptr;
   cudaEvent_t ev_copied[2] = {nullptr, nullptr};
   cudaEvent_t ev_consumed[2] = {nullptr, nullptr};
-  int prepared_smem[2] = {0, 0};  // largest dynamic smem set per kernel variant
-  // (aggregate, P, threads, smem) -> resident clusters
-  std::map<std::tuple<int, int, int, int>, int> occupancy;
+  // Largest dynamic shared memory set so far per kernel variant: direct
+  // (aggregate 0/1), ship (4 / 8 keys per thread).
+  int prepared_direct[2] = {0, 0};
+  int prepared_ship[2] = {0, 0};
+  // (kernel, variant, P, threads, smem) -> resident clusters
+  std::map<std::tuple<int, int, int, int, int>, int> occupancy;
   std::mutex host_call;  // serialises dsmem_hist_host on this device
 };
 
@@ -114,18 +117,44 @@ int ensure_pool(DeviceState* st) {
   return DSMEM_HIST_OK;
 }
 
+// Sets the dynamic shared-memory attribute a plan's kernel needs (once per
+// size increase).  g_mutex must be held.
+int prepare_locked(DeviceState* st, const dsmem_hist_plan_t& p) {
+  cudaError_t e = cudaSuccess;
+  if (p.kernel == DSMEM_HIST_KERNEL_SHIP) {
+    const int v = p.keys_per_thread == 8 ? 1 : 0;
+    if (p.smem_bytes > st->prepared_ship[v]) {
+      if ((e = prepare_ship_kernel(p.keys_per_thread, p.smem_bytes)) != cudaSuccess)
+        return fail_cuda(e, "cudaFuncSetAttribute");
+      st->prepared_ship[v] = p.smem_bytes;
+    }
+  } else if (p.smem_bytes > st->prepared_direct[p.aggregate]) {
+    if ((e = prepare_cluster_kernel(p.aggregate, p.smem_bytes)) != cudaSuccess)
+      return fail_cuda(e, "cudaFuncSetAttribute");
+    st->prepared_direct[p.aggregate] = p.smem_bytes;
+  }
+  return DSMEM_HIST_OK;
+}
+
+cudaError_t launch_plan(const dsmem_hist_plan_t& plan, const ClusterHistArgs& args,
+                        cudaStream_t stream) {
+  if (plan.kernel == DSMEM_HIST_KERNEL_SHIP) return launch_cluster_ship(plan, args, stream);
+  return launch_cluster_hist(plan, args, stream);
+}
+
 // Plans for the current device, confirming the shape with the occupancy
 // API; in automatic mode a cluster size the device cannot hold is halved
 // (more passes) until one fits.  g_mutex must be held.
 int plan_locked(DeviceState* st, int32_t num_bins, int64_t n, const dsmem_hist_request_t* req_in,
                 dsmem_hist_plan_t* out) {
-  dsmem_hist_request_t req = {0, 0, 0, -1, 0};
+  dsmem_hist_request_t req = {0, 0, 0, -1, 0, -1};
   if (req_in) req = *req_in;
   // Environment overrides for sweeps (only where the caller left a field open).
   if (req.cluster_size == 0) req.cluster_size = env_int("DSMEM_HIST_CLUSTER", 0);
   if (req.block_threads == 0) req.block_threads = env_int("DSMEM_HIST_BLOCK", 0);
   if (req.num_clusters == 0) req.num_clusters = env_int("DSMEM_HIST_GRID", 0);
   if (req.aggregate < 0) req.aggregate = env_int("DSMEM_HIST_AGGREGATE", -1);
+  if (req.kernel < 0) req.kernel = env_int("DSMEM_HIST_KERNEL", -1);
 
   dsmem_hist_device_t dev = st->dev;
   for (;;) {
@@ -133,20 +162,20 @@ int plan_locked(DeviceState* st, int32_t num_bins, int64_t n, const dsmem_hist_r
     int rc = plan_shape(&dev, num_bins, n, &req, 0, out, &why);
     if (rc != DSMEM_HIST_OK) return fail(rc, "plan: %s", why);
     cudaError_t e;
-    const int agg = out->aggregate;
-    if (out->smem_bytes > st->prepared_smem[agg]) {
-      if ((e = prepare_cluster_kernel(agg, out->smem_bytes)) != cudaSuccess)
-        return fail_cuda(e, "cudaFuncSetAttribute");
-      st->prepared_smem[agg] = out->smem_bytes;
-    }
-    auto key = std::make_tuple(agg, out->cluster_size, out->block_threads, out->smem_bytes);
+    if ((rc = prepare_locked(st, *out))) return rc;
+    const bool ship = out->kernel == DSMEM_HIST_KERNEL_SHIP;
+    const int variant = ship ? out->keys_per_thread : out->aggregate;
+    auto key = std::make_tuple(out->kernel, variant, out->cluster_size, out->block_threads,
+                               out->smem_bytes);
     auto it = st->occupancy.find(key);
     int mac = 0;
     if (it != st->occupancy.end()) {
       mac = it->second;
     } else {
-      e = query_max_active_clusters(agg, out->cluster_size, out->block_threads, out->smem_bytes,
-                                    &mac);
+      e = ship ? query_ship_active_clusters(out->keys_per_thread, out->cluster_size,
+                                            out->smem_bytes, &mac)
+               : query_max_active_clusters(out->aggregate, out->cluster_size, out->block_threads,
+                                           out->smem_bytes, &mac);
       if (e != cudaSuccess) {
         cudaGetLastError();  // clear the sticky-free error of a refused shape
         mac = 0;
@@ -158,6 +187,10 @@ int plan_locked(DeviceState* st, int32_t num_bins, int64_t n, const dsmem_hist_r
       if (rc != DSMEM_HIST_OK) return fail(rc, "plan: %s", why);
       break;
     }
+    if (out->kernel == DSMEM_HIST_KERNEL_SHIP && req.kernel < 0) {
+      req.kernel = DSMEM_HIST_KERNEL_DIRECT;  // shipping shape not resident: try direct
+      continue;
+    }
     if (req.cluster_size != 0 || out->cluster_size <= 1)
       return fail(DSMEM_HIST_EUNSUPPORTED,
                   "cluster of %d CTAs x %d threads x %d B shared memory cannot be resident",
@@ -166,10 +199,12 @@ int plan_locked(DeviceState* st, int32_t num_bins, int64_t n, const dsmem_hist_r
   }
   if (trace_enabled())
     fprintf(stderr,
-            "[dsmem_hist] bins=%d n=%lld -> P=%d S=%d passes=%d threads=%d C=%d smem=%d agg=%d "
-            "ctas/SM=%d max_active_clusters=%d scratch=%lld B\n",
-            num_bins, static_cast<long long>(n), out->cluster_size, out->bins_per_cta,
-            out->passes, out->block_threads, out->num_clusters, out->smem_bytes, out->aggregate,
+            "[dsmem_hist] bins=%d n=%lld -> kernel=%s P=%d S=%d passes=%d threads=%d C=%d "
+            "smem=%d agg=%d kpt=%d nq=%d ctas/SM=%d max_active_clusters=%d scratch=%lld B\n",
+            num_bins, static_cast<long long>(n),
+            out->kernel == DSMEM_HIST_KERNEL_SHIP ? "ship" : "direct", out->cluster_size,
+            out->bins_per_cta, out->passes, out->block_threads, out->num_clusters,
+            out->smem_bytes, out->aggregate, out->keys_per_thread, out->sub_vectors,
             out->ctas_per_sm, out->max_active_clusters,
             static_cast<long long>(out->workspace_bytes));
   return DSMEM_HIST_OK;
@@ -203,6 +238,7 @@ ClusterHistArgs make_args(const dsmem_hist_plan_t& plan, const int32_t* keys, in
   a.stride = static_cast<uint64_t>(plan.partial_stride);
   a.head = head_keys(keys, n);
   a.accumulate = static_cast<uint32_t>(accumulate);
+  a.sub_vectors = static_cast<uint32_t>(plan.sub_vectors);
   return a;
 }
 
@@ -232,7 +268,7 @@ int run_device(const int32_t* keys, int64_t n, int32_t num_bins, uint32_t* bins,
   }
   uint32_t* partials = static_cast<uint32_t*>(scratch);
   const ClusterHistArgs args = make_args(plan, keys, n, num_bins, partials, 0);
-  e = launch_cluster_hist(plan, args, stream);
+  e = launch_plan(plan, args, stream);
   if (e == cudaSuccess)
     e = launch_reduce_partials(partials, args.stride, static_cast<uint32_t>(plan.num_clusters),
                                args.num_bins, bins, stream);
@@ -248,7 +284,16 @@ int check_plan(const DeviceState* st, const dsmem_hist_plan_t* p, int32_t num_bi
   const int64_t P = p->cluster_size, S = p->bins_per_cta;
   if (P < 1 || P > 16 || P > st->dev.max_cluster_size)
     return fail(DSMEM_HIST_EINVAL, "plan: cluster_size %lld out of range", static_cast<long long>(P));
-  if (S < 4 || (S & 3) || S >= (int64_t{1} << 18) || p->smem_bytes != 4 * S ||
+  if (p->kernel == DSMEM_HIST_KERNEL_SHIP) {
+    const int nq = p->sub_vectors;
+    if (P < 2 || p->block_threads != 1024 || (p->keys_per_thread != 4 && p->keys_per_thread != 8) ||
+        nq < 1 || nq > 32 || S + 32 >= 0xFFFF ||
+        p->smem_bytes != 4 * S + static_cast<int64_t>(ship_staging_bytes(static_cast<int>(P), nq)))
+      return fail(DSMEM_HIST_EINVAL, "plan: ship kernel fields inconsistent");
+  } else if (p->kernel != DSMEM_HIST_KERNEL_DIRECT || p->smem_bytes != 4 * S) {
+    return fail(DSMEM_HIST_EINVAL, "plan: kernel / smem_bytes inconsistent");
+  }
+  if (S < 4 || (S & 3) || S >= (int64_t{1} << 18) ||
       p->smem_bytes > st->dev.max_smem_per_block_optin)
     return fail(DSMEM_HIST_EINVAL, "plan: bins_per_cta / smem_bytes inconsistent");
   if (p->passes < 1 || static_cast<int64_t>(p->passes) * P * S < num_bins ||
@@ -275,14 +320,10 @@ int run_partials(const int32_t* keys, int64_t n, int32_t num_bins, const dsmem_h
     DeviceState* st = nullptr;
     if ((rc = device_state(&st))) return rc;
     if ((rc = check_plan(st, plan, num_bins))) return rc;
-    if (plan->smem_bytes > st->prepared_smem[plan->aggregate]) {
-      const cudaError_t e = prepare_cluster_kernel(plan->aggregate, plan->smem_bytes);
-      if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute");
-      st->prepared_smem[plan->aggregate] = plan->smem_bytes;
-    }
+    if ((rc = prepare_locked(st, *plan))) return rc;
   }
   const ClusterHistArgs args = make_args(*plan, keys, n, num_bins, partials, accumulate);
-  const cudaError_t e = launch_cluster_hist(*plan, args, stream);
+  const cudaError_t e = launch_plan(*plan, args, stream);
   return e == cudaSuccess ? DSMEM_HIST_OK : fail_cuda(e, "cluster histogram launch");
 }
 
@@ -365,7 +406,7 @@ int run_host(const int32_t* h_keys, int64_t n, int32_t num_bins, uint32_t* h_bin
       break;
     }
     const ClusterHistArgs args = make_args(plan, stage[b], cnt, num_bins, partials, j > 0);
-    if ((e = launch_cluster_hist(plan, args, stream)) != cudaSuccess ||
+    if ((e = launch_plan(plan, args, stream)) != cudaSuccess ||
         (e = cudaEventRecord(st->ev_consumed[b], stream)) != cudaSuccess) {
       rc = fail_cuda(e, "cluster histogram launch");
       break;

@@ -36,6 +36,7 @@ struct ClusterHistArgs {
   uint64_t stride;      // partial row stride (u32 elements, multiple of 4)
   uint32_t head;        // keys before the first 16-byte boundary of `keys` (0..3, <= n)
   uint32_t accumulate;  // 1: add the slice into the partial row, 0: overwrite it
+  uint32_t sub_vectors; // ship kernel: 16-byte vectors per sub-bucket (power of two)
 };
 
 // Launches (all asynchronous on `stream`).
@@ -46,6 +47,14 @@ cudaError_t launch_reduce_partials(const uint32_t* partials, uint64_t stride,
                                    cudaStream_t stream);
 cudaError_t launch_global_atomic(const int32_t* keys, int64_t n, uint32_t num_bins,
                                  uint32_t* bins, cudaStream_t stream);
+
+// Ship kernel (cluster_ship.cu; its staging size is computed by the planner).
+uint32_t ship_staging_bytes(int cluster_size, int sub_vectors);
+cudaError_t prepare_ship_kernel(int keys_per_thread, int smem_bytes);
+cudaError_t query_ship_active_clusters(int keys_per_thread, int cluster_size, int smem_bytes,
+                                       int* out);
+cudaError_t launch_cluster_ship(const dsmem_hist_plan_t& plan, const ClusterHistArgs& args,
+                                cudaStream_t stream);
 
 // Sets the kernel attributes a shape needs (dynamic shared memory above
 // 48 KiB, non-portable cluster sizes) on the current device.

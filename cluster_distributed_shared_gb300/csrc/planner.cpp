@@ -14,7 +14,12 @@
 //             rounded up to a multiple of 4 (the page's kernel needs
 //             P * S == num_bins exactly; here the last CTA's slice may have
 //             a few never-hit counters instead, and no bin is dropped)
-//   threads = 1024 when only one CTA fits an SM, else 512
+//   kernel  = SHIP (keys shipped to owners as 16-bit indices, local atomics)
+//             when P >= 2 and the slice plus its staging fit one CTA: 8 keys
+//             per thread per round if that fits, else 4, with sub-buckets
+//             holding twice (else 1.5 times) the expected entries; else DIRECT
+//   threads = 1024 for SHIP; for DIRECT 1024 when only one CTA fits an SM,
+//             else 512
 //   C       = min(resident clusters, clusters needed so each CTA gets at
 //             least kMinStepsPerCta unrolled steps of keys, clusters whose
 //             partial rows fit kMaxAutoScratchBytes), at least 1
@@ -25,6 +30,18 @@
 namespace dsmh {
 
 uint64_t owner_magic(uint32_t S) { return ((uint64_t{1} << 40) / S) + 1; }
+
+// Shared memory the ship kernel needs beside the slice; the kernel lays it
+// out in this order: 32 dummy counters after the slice (targets of padding
+// entries), cursors u32[P*32], inbox headers u32[2][16], sub-buckets [P][32]
+// of 2*qs + 4 bytes (qs = 8*sub_vectors entries; total rounded up to 16
+// bytes), inboxes uint4[2][P][32*sub_vectors].
+uint32_t ship_staging_bytes(int cluster_size, int sub_vectors) {
+  const uint32_t P = static_cast<uint32_t>(cluster_size), nq = static_cast<uint32_t>(sub_vectors);
+  const uint32_t buckets = (P * 32u * (16u * nq + 4u) + 15u) & ~15u;
+  return 4u * 32u + 4u * 32u * P + 4u * 32u + buckets + 16u * 2u * P * 32u * nq;
+}
+
 
 static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -38,7 +55,7 @@ static int ctas_per_sm(const dsmem_hist_device_t* dev, int smem_bytes, int threa
 int plan_shape(const dsmem_hist_device_t* dev, int32_t num_bins, int64_t n,
                const dsmem_hist_request_t* req, int32_t max_active_clusters,
                dsmem_hist_plan_t* out, const char** why) {
-  static const dsmem_hist_request_t kNoRequest = {0, 0, 0, -1, 0};
+  static const dsmem_hist_request_t kNoRequest = {0, 0, 0, -1, 0, -1};
   if (!req) req = &kNoRequest;
   *why = "";
   if (!dev || !out) { *why = "null device or plan pointer"; return DSMEM_HIST_EINVAL; }
@@ -81,14 +98,55 @@ int plan_shape(const dsmem_hist_device_t* dev, int32_t num_bins, int64_t n,
   const int64_t passes = ceil_div(num_bins, P * s_max);
   int64_t S = ceil_div(ceil_div(num_bins, passes), P);
   S = (S + 3) & ~int64_t{3};
-  const int smem = static_cast<int>(4 * S);
+  int smem = static_cast<int>(4 * S);
+
+  if (req->block_threads != 0 &&
+      (req->block_threads < 64 || req->block_threads > 1024 || (req->block_threads & 31))) {
+    *why = "block_threads must be a multiple of 32 in [64, 1024]";
+    return DSMEM_HIST_EINVAL;
+  }
+  if (req->kernel < -1 || req->kernel > DSMEM_HIST_KERNEL_SHIP) {
+    *why = "kernel must be -1, DSMEM_HIST_KERNEL_DIRECT or DSMEM_HIST_KERNEL_SHIP";
+    return DSMEM_HIST_EINVAL;
+  }
+  // Kernel choice: shipping whenever the cluster has remote owners and its
+  // staging fits beside the slice (1024 threads), else direct increments.
+  int kernel = DSMEM_HIST_KERNEL_DIRECT, kpt = 0, nq = 0;
+  const bool ship_ok_threads = req->block_threads == 0 || req->block_threads == 1024;
+  if (req->kernel == DSMEM_HIST_KERNEL_SHIP || (req->kernel < 0 && P >= 2 && ship_ok_threads)) {
+    if (P < 2 || !ship_ok_threads) {
+      if (req->kernel == DSMEM_HIST_KERNEL_SHIP) {
+        *why = "the ship kernel needs cluster_size >= 2 and 1024 threads";
+        return DSMEM_HIST_EINVAL;
+      }
+    } else {
+      // Sub-bucket capacity: twice the expected 32*k/P entries per round, else
+      // 1.5 times (rounded up to whole 8-entry vectors); 8 keys per thread and
+      // round before 4.
+      for (int t = 0; t < 4 && !kernel; ++t) {
+        const int k = t < 2 ? 8 : 4;
+        const int64_t expect = 32 * k;  // entries per sub-bucket per round, times P
+        const int q = static_cast<int>(ceil_div((t % 2 == 0 ? 2 * expect : 3 * expect / 2), 8 * P));
+        const int64_t need = 4 * S + ship_staging_bytes(P, q);
+        if (need <= dev->max_smem_per_block_optin &&
+            need + kSmemReservedPerCta <= dev->max_smem_per_sm) {
+          kernel = DSMEM_HIST_KERNEL_SHIP;
+          kpt = k;
+          nq = q;
+          smem = static_cast<int>(need);
+        }
+      }
+      if (!kernel && req->kernel == DSMEM_HIST_KERNEL_SHIP) {
+        *why = "slice plus ship staging exceed the shared memory of one CTA";
+        return DSMEM_HIST_EUNSUPPORTED;
+      }
+    }
+  }
 
   int threads;
-  if (req->block_threads != 0) {
-    if (req->block_threads < 64 || req->block_threads > 1024 || (req->block_threads & 31)) {
-      *why = "block_threads must be a multiple of 32 in [64, 1024]";
-      return DSMEM_HIST_EINVAL;
-    }
+  if (kernel == DSMEM_HIST_KERNEL_SHIP) {
+    threads = 1024;
+  } else if (req->block_threads != 0) {
     threads = req->block_threads;
   } else {
     threads = ctas_per_sm(dev, smem, 512) <= 1 ? 1024 : 512;
@@ -130,7 +188,13 @@ int plan_shape(const dsmem_hist_device_t* dev, int32_t num_bins, int64_t n,
   out->block_threads = threads;
   out->num_clusters = static_cast<int32_t>(C);
   out->smem_bytes = smem;
-  out->aggregate = req->aggregate >= 0 ? (req->aggregate ? 1 : 0) : 1;
+  // Direct kernel: __match_any_sync aggregation only on request (it costs
+  // about as much as a remote increment on GB300).  Ship kernel: whole-tile
+  // aggregation of runs is always on.
+  out->aggregate = kernel == DSMEM_HIST_KERNEL_SHIP ? 1 : (req->aggregate > 0 ? 1 : 0);
+  out->kernel = kernel;
+  out->keys_per_thread = kpt;
+  out->sub_vectors = nq;
   out->ctas_per_sm = per_sm;
   out->max_active_clusters = max_active_clusters > 0 ? max_active_clusters : 0;
   out->reserved = 0;

@@ -1,0 +1,117 @@
+// Inline-PTX helpers for the cluster kernels (sm_90 and later; written for
+// sm_103a).  Cluster special registers, the release/acquire cluster barrier,
+// shared::cta -> shared::cluster address mapping, remote reductions and
+// stores, and streaming 16-byte global loads.
+#pragma once
+
+#include <stdint.h>
+
+namespace dsmh {
+namespace ptx {
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+
+// Full cluster barrier.  The release half orders this thread's earlier
+// shared-memory writes, remote stores and remote reductions before its
+// arrival; the acquire half makes every other thread's such writes visible
+// after the wait.
+__device__ __forceinline__ void cluster_barrier() {
+  __syncwarp();
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The two halves, for overlapping the barrier's latency with local work.
+__device__ __forceinline__ void cluster_arrive() {
+  __syncwarp();
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+// Arrival without release ordering: for threads that published no remote
+// writes since the last phase.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  __syncwarp();
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  __syncwarp();
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Barrier among `count` threads (a multiple of 32) of this CTA on hardware
+// barrier `id` (0 is the one __syncthreads uses).
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+// shared::cta address of this CTA -> shared::cluster address of the same
+// offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void red_add_cluster(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v));
+}
+__device__ __forceinline__ void red_add_local(uint32_t cta_addr, uint32_t v) {
+  asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(cta_addr), "r"(v));
+}
+__device__ __forceinline__ uint32_t atom_add_local(uint32_t cta_addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.shared.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(cta_addr), "r"(v));
+  return old;
+}
+__device__ __forceinline__ uint16_t ld_shared_u16(uint32_t cta_addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(cta_addr));
+  return v;
+}
+
+// Asm statements without a "memory" clobber are still volatile, so they keep
+// their order relative to each other and to the barriers above (which do
+// clobber memory); plain C++ shared-memory accesses are separated from them by
+// those barriers.
+__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, const uint4& v) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w));
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v));
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t cta_addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(cta_addr));
+  return v;
+}
+__device__ __forceinline__ void st_shared_u16(uint32_t cta_addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(cta_addr), "h"(v));
+}
+__device__ __forceinline__ int4 ld_stream_v4(const int4* p) {
+  int4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.s32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+}  // namespace ptx
+}  // namespace dsmh

@@ -55,6 +55,14 @@ enum {
   DSMEM_HIST_ENOMEM = -5        /* the scratch pool could not supply the partial histograms */
 };
 
+/* How increments reach a remote owner's slice.
+ *   DIRECT: one `red.shared::cluster` per key (the page's kernel, optionally
+ *           with __match_any_sync warp aggregation).
+ *   SHIP:   keys travel to their owner as 16-bit local indices in coalesced
+ *           16-byte DSMEM stores and the owner applies local shared-memory
+ *           atomics (1024 threads per CTA; P >= 2). */
+enum { DSMEM_HIST_KERNEL_DIRECT = 0, DSMEM_HIST_KERNEL_SHIP = 1 };
+
 /* Launch shape chosen by the planner (all fields filled by dsmem_hist_plan*). */
 typedef struct dsmem_hist_plan {
   int32_t cluster_size;        /* P: CTAs per cluster, 1..16 (16 is non-portable) */
@@ -63,22 +71,26 @@ typedef struct dsmem_hist_plan {
                                   num_bins exceeds what one cluster holds) */
   int32_t block_threads;       /* threads per CTA */
   int32_t num_clusters;        /* C: clusters launched (persistent grid of C*P CTAs) */
-  int32_t smem_bytes;          /* dynamic shared memory per CTA: 4*S */
+  int32_t smem_bytes;          /* dynamic shared memory per CTA: 4*S (+ staging for SHIP) */
   int32_t aggregate;           /* 1: warp pre-aggregation of equal keys (__match_any_sync + popc) */
   int32_t ctas_per_sm;         /* resident CTAs per SM the shape allows */
   int32_t max_active_clusters; /* occupancy answer for this shape (0 when not queried) */
+  int32_t kernel;              /* DSMEM_HIST_KERNEL_DIRECT or DSMEM_HIST_KERNEL_SHIP */
+  int32_t keys_per_thread;     /* ship kernel: keys each thread partitions per round (4 or 8) */
+  int32_t sub_vectors;         /* ship kernel: 16-byte vectors per (owner, lane) sub-bucket */
   int32_t reserved;            /* zero */
   int64_t partial_stride;      /* u32 elements between two clusters' partial rows (num_bins rounded up to 4) */
   int64_t workspace_bytes;     /* scratch: num_clusters * partial_stride * 4 */
 } dsmem_hist_plan_t;
 
-/* Planner overrides; a zero field (or -1 for `aggregate`) means "choose". */
+/* Planner overrides; a zero field (or -1 for `aggregate` and `kernel`) means "choose". */
 typedef struct dsmem_hist_request {
   int32_t cluster_size;    /* force P (1..16) */
   int32_t block_threads;   /* force threads per CTA (multiple of 32, 64..1024) */
   int32_t num_clusters;    /* force C */
   int32_t aggregate;       /* -1 choose, 0 off, 1 on */
   int32_t max_slice_bytes; /* cap on 4*S (default 128 KiB) */
+  int32_t kernel;          /* -1 choose, else DSMEM_HIST_KERNEL_* */
 } dsmem_hist_request_t;
 
 /* The device facts the planner uses; filled from cudaGetDeviceProperties by

@@ -82,9 +82,12 @@ def plan(dev, nb, n, mac=0, **kw):
 def test_planner_matches_published_cluster_shapes(nb, n, P, S):
     p = plan(GB300, nb, n, cluster_size=P)
     assert (p["cluster_size"], p["bins_per_cta"], p["passes"]) == (P, S, 1)
-    assert p["smem_bytes"] == 4 * S
+    assert p["kernel"] == pkg.KERNEL_SHIP and p["block_threads"] == 1024
+    assert 4 * S < p["smem_bytes"] <= GB300["max_smem_per_block_optin"]
     q = plan(GB300, nb, n)          # the planner's own choice agrees here
     assert (q["cluster_size"], q["bins_per_cta"]) == (P, S)
+    d = plan(GB300, nb, n, cluster_size=P, kernel=pkg.KERNEL_DIRECT)
+    assert d["kernel"] == pkg.KERNEL_DIRECT and d["smem_bytes"] == 4 * S
 
 
 @pytest.mark.parametrize("nb", [1, 2, 3, 5, 97, 4095, 4096, 4097, 65535, 65537, 100003, 262143,
@@ -102,8 +105,34 @@ def test_planner_covers_every_bin(nb, slice_cap):
         assert P * S < 2 ** 20 + 16 * 4                    # owner arithmetic range
         assert p["partial_stride"] % 4 == 0 and p["partial_stride"] >= nb
         assert p["workspace_bytes"] == p["num_clusters"] * p["partial_stride"] * 4
+        assert p["smem_bytes"] <= GB300["max_smem_per_block_optin"]
+        if p["kernel"] == pkg.KERNEL_SHIP:
+            assert P >= 2 and p["block_threads"] == 1024 and p["keys_per_thread"] in (4, 8)
+            nq = p["sub_vectors"]
+            assert nq >= 1 and 8 * nq * 32 * P >= 1.5 * 1024 * p["keys_per_thread"]
+            assert p["smem_bytes"] == 4 * S + ship_staging(P, nq)
+            assert S < 0xFFFF                               # 16-bit local indices + sentinel
+        else:
+            assert p["smem_bytes"] == 4 * S
         if forced:
             assert P == forced
+
+
+def ship_staging(P, nq):
+    # dummy counters, cursors, headers, skewed sub-buckets, double inbox
+    buckets = (P * 32 * (16 * nq + 4) + 15) // 16 * 16
+    return 4 * 32 + 4 * 32 * P + 4 * 32 + buckets + 16 * 2 * P * 32 * nq
+
+
+@pytest.mark.parametrize("P", range(2, 17))
+def test_ship_plan_fits_for_every_cluster_size(P):
+    for nb in (P * 4, P * 32768, 262144, 524288):
+        p = plan(GB300, nb, 1 << 26, cluster_size=P, kernel=pkg.KERNEL_SHIP)
+        assert p["kernel"] == pkg.KERNEL_SHIP
+        assert p["smem_bytes"] + 1024 <= GB300["max_smem_per_sm"]
+        # sub-buckets hold at least 1.5 times the expected keys per (owner, lane) and round
+        expected = 32 * p["keys_per_thread"] / P
+        assert 8 * p["sub_vectors"] >= 1.5 * expected
 
 
 def test_owner_magic_exact():
@@ -122,7 +151,11 @@ def test_planner_grid_and_threads():
     p = plan(GB300, 262144, 1 << 28, mac=16)
     assert p["num_clusters"] == 16 and p["block_threads"] == 1024 and p["ctas_per_sm"] == 1
     small = plan(GB300, 8192, 1000, mac=100)
-    assert small["num_clusters"] == 1 and small["block_threads"] == 512
+    assert small["num_clusters"] == 1 and small["block_threads"] == 1024
+    direct = plan(GB300, 8192, 1000, mac=100, kernel=pkg.KERNEL_DIRECT)
+    assert direct["block_threads"] == 512 and direct["kernel"] == pkg.KERNEL_DIRECT
+    one = plan(GB300, 8192, 1 << 20, cluster_size=1)
+    assert one["kernel"] == pkg.KERNEL_DIRECT      # no remote owners: local increments
     forced = plan(GB300, 8192, 1 << 20, mac=100, num_clusters=7, block_threads=256)
     assert forced["num_clusters"] == 7 and forced["block_threads"] == 256
 
@@ -152,6 +185,15 @@ def test_planner_errors():
         plan(GB300, 0, 10)
 
 
-def test_aggregate_override():
-    assert plan(GB300, 4096, 1 << 20, aggregate=0)["aggregate"] == 0
-    assert plan(GB300, 4096, 1 << 20, aggregate=1)["aggregate"] == 1
+def test_aggregate_and_kernel_overrides():
+    d = pkg.KERNEL_DIRECT
+    assert plan(GB300, 4096, 1 << 20, aggregate=0, kernel=d)["aggregate"] == 0
+    assert plan(GB300, 4096, 1 << 20, aggregate=1, kernel=d)["aggregate"] == 1
+    assert plan(GB300, 4096, 1 << 20, kernel=d)["aggregate"] == 0
+    assert plan(GB300, 4096, 1 << 20)["kernel"] == pkg.KERNEL_SHIP
+    assert plan(GB300, 4096, 1 << 20, block_threads=256)["kernel"] == d
+    for bad in [dict(kernel=pkg.KERNEL_SHIP, cluster_size=1),
+                dict(kernel=pkg.KERNEL_SHIP, block_threads=256), dict(kernel=7)]:
+        with pytest.raises(pkg.DsmemHistError) as e:
+            plan(GB300, 4096, 1 << 20, **bad)
+        assert e.value.code == pkg.DSMEM_HIST_EINVAL

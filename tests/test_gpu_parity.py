@@ -73,10 +73,15 @@ def test_pins_default_plan(pin):
     pin(gpu_hist)
 
 
+D, SH = pkg.KERNEL_DIRECT, pkg.KERNEL_SHIP
+
+
 @pytest.mark.parametrize("shape", [
-    dict(cluster_size=1, aggregate=0), dict(cluster_size=2, aggregate=1),
-    dict(cluster_size=4, aggregate=0, block_threads=256), dict(cluster_size=8, aggregate=1),
-    dict(cluster_size=16, aggregate=0), dict(cluster_size=16, aggregate=1, block_threads=64),
+    dict(cluster_size=1, aggregate=0), dict(cluster_size=2, aggregate=1, kernel=D),
+    dict(cluster_size=4, aggregate=0, block_threads=256), dict(cluster_size=8, aggregate=1, kernel=D),
+    dict(cluster_size=16, aggregate=0, kernel=D), dict(cluster_size=16, aggregate=1, block_threads=64),
+    dict(cluster_size=2, kernel=SH), dict(cluster_size=3, kernel=SH), dict(cluster_size=8, kernel=SH),
+    dict(cluster_size=16, kernel=SH), dict(cluster_size=5, kernel=SH, num_clusters=1),
 ], ids=str)
 @pytest.mark.parametrize("pin", [pins.pin_brute_force_tiny, pins.pin_cycle,
                                  pins.pin_constructed_counts, pins.pin_single_value,
@@ -103,29 +108,51 @@ def test_forced_shape_sweep(num_bins):
         keys_np = base[off:off + n]
         want = oracle.histogram(keys_np, num_bins)
         keys = dev[off:off + n]
-        for P in (1, 2, 4, 8, 16):
-            for agg in (0, 1):
-                for threads in (256, 1024):
-                    got = pkg.dsmem_hist(keys, num_bins, cluster_size=P, aggregate=agg,
-                                         block_threads=threads)
-                    torch.cuda.synchronize()
-                    g = to_np(got)
-                    assert np.array_equal(g, want), (num_bins, off, P, agg, threads,
-                                                     np.flatnonzero(g != want)[:8])
+        shapes = [dict(cluster_size=P, kernel=D, aggregate=agg, block_threads=t)
+                  for P in (1, 2, 4, 8, 16) for agg in (0, 1) for t in (256, 1024)]
+        shapes += [dict(cluster_size=P, kernel=SH) for P in (2, 3, 4, 6, 8, 12, 16)]
+        for kw in shapes:
+            got = pkg.dsmem_hist(keys, num_bins, **kw)
+            torch.cuda.synchronize()
+            g = to_np(got)
+            assert np.array_equal(g, want), (num_bins, off, kw, np.flatnonzero(g != want)[:8])
 
 
-@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 31, 32, 33, 127, 128, 129, 130, 511, 4099, 65537])
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 31, 32, 33, 127, 128, 129, 130, 511, 4099, 65537,
+                               2 * 128 * 32 * 6 + 5, 1 << 20])
 def test_ragged_small_lengths(n):
     num_bins = 37
     base = gen.uniform(n + 3, 40, seed=n)
     dev = torch.from_numpy(base).cuda()
     for off in (0, 1, 2, 3):
         want = oracle.histogram(base[off:off + n], num_bins)
-        for agg in (0, 1):
-            got = pkg.dsmem_hist(dev[off:off + n], num_bins, cluster_size=2, aggregate=agg,
-                                 num_clusters=3)
+        for kw in (dict(kernel=D, aggregate=0), dict(kernel=D, aggregate=1), dict(kernel=SH)):
+            got = pkg.dsmem_hist(dev[off:off + n], num_bins, cluster_size=2, num_clusters=3, **kw)
             torch.cuda.synchronize()
-            assert np.array_equal(to_np(got), want), (n, off, agg)
+            assert np.array_equal(to_np(got), want), (n, off, kw)
+
+
+def test_ship_overflow_and_runs_paths():
+    # Keys that all belong to one owner overflow its sub-buckets (remote
+    # increments take over); runs of equal keys take the whole-tile path;
+    # partial runs and run boundaries mix both.
+    rng = np.random.default_rng(3)
+    n = 1 << 22
+    cases = []
+    cases.append((rng.integers(0, 32768, n).astype(np.int32), 262144, 8))      # owner 0 only
+    cases.append((rng.integers(7 * 32768, 8 * 32768, n).astype(np.int32), 262144, 8))  # last owner
+    runs = np.repeat(rng.integers(0, 524288, n // 128), 128).astype(np.int32)
+    cases.append((runs, 524288, 16))
+    odd = np.repeat(rng.integers(0, 65536, n // 37 + 1), 37)[:n].astype(np.int32)
+    cases.append((odd, 65536, 2))
+    mix = rng.integers(0, 262144, n).astype(np.int32)
+    mix[: n // 2] = 12345                                                       # one hot bin
+    cases.append((mix, 262144, 8))
+    for keys, num_bins, P in cases:
+        want = oracle.histogram(keys, num_bins)
+        for kw in (dict(kernel=SH), dict(kernel=D)):
+            got = gpu_hist(keys, num_bins, cluster_size=P, **kw)
+            assert np.array_equal(got, want), (num_bins, P, kw)
 
 
 def test_multi_pass_bin_ranges():
@@ -173,13 +200,15 @@ def test_workload_full_size(name, seed):
         torch.cuda.synchronize()
         got = to_np(out)
         assert np.array_equal(got, want), (name, seed, kw, np.flatnonzero(got != want)[:8])
+    assert plan["kernel"] == SH
     if seed == 0:
         pkg.dsmem_hist_global_atomic(d, num_bins, out=out)
         torch.cuda.synchronize()
         assert np.array_equal(to_np(out), want)
-        pkg.dsmem_hist(d, num_bins, out=out, cluster_size=P, aggregate=1 - plan["aggregate"])
-        torch.cuda.synchronize()
-        assert np.array_equal(to_np(out), want)
+        for agg in (0, 1):
+            pkg.dsmem_hist(d, num_bins, out=out, cluster_size=P, kernel=D, aggregate=agg)
+            torch.cuda.synchronize()
+            assert np.array_equal(to_np(out), want), agg
     del d
     torch.cuda.empty_cache()
 
@@ -223,7 +252,8 @@ def test_repeat_is_deterministic_across_shapes():
     d = torch.from_numpy(keys).cuda()
     for i in range(5):
         for kw in (dict(cluster_size=2), dict(cluster_size=4, num_clusters=1),
-                   dict(cluster_size=8, num_clusters=64), dict(aggregate=0), dict(aggregate=1)):
+                   dict(cluster_size=8, num_clusters=64), dict(kernel=D, aggregate=0),
+                   dict(kernel=D, aggregate=1), dict(kernel=SH, cluster_size=16, num_clusters=40)):
             got = pkg.dsmem_hist(d, num_bins, **kw)
             torch.cuda.synchronize()
             assert np.array_equal(to_np(got), want), kw
