@@ -84,7 +84,7 @@ class Device(ctypes.Structure):
 
 EXPORTS = (
     "dsmem_hist", "dsmem_hist_ex", "dsmem_hist_global_atomic", "dsmem_hist_host",
-    "dsmem_hist_partials", "dsmem_hist_reduce",
+    "dsmem_hist_partials", "dsmem_hist_reduce", "dsmem_hist_static",
     "dsmem_hist_plan", "dsmem_hist_plan_for_device", "dsmem_hist_strerror",
     "dsmem_hist_last_error", "dsmem_hist_release", "dsmem_hist_version",
 )
@@ -110,6 +110,7 @@ def lib():
                 ("dsmem_hist", [p, i64, i32, p, p]),
                 ("dsmem_hist_ex", [p, i64, i32, p, ctypes.POINTER(Request), p]),
                 ("dsmem_hist_global_atomic", [p, i64, i32, p, p]),
+                ("dsmem_hist_static", [p, i64, i32, p, p]),
                 ("dsmem_hist_host", [p, i64, i32, p, p]),
                 ("dsmem_hist_partials", [p, i64, i32, ctypes.POINTER(Plan), p, i32, p]),
                 ("dsmem_hist_reduce", [p, i32, i64, i32, p, p]),
@@ -207,6 +208,21 @@ def dsmem_hist_ex(keys, num_bins: int, request: Request, out=None, stream=None):
     with torch.cuda.device(keys.device):
         _check(lib().dsmem_hist_ex(keys.data_ptr(), keys.numel(), int(num_bins), out.data_ptr(),
                                    ctypes.byref(request), _stream_handle(stream)))
+    return out
+
+
+def dsmem_hist_static(keys, num_bins: int, out=None, stream=None):
+    """dsmem_hist without any allocation by the library: the partial rows
+    live in the library's fixed 32 MiB static device array (num_bins up to
+    8,388,608).  For callers that cannot let a library allocate (stream
+    capture, caller-owned memory arenas, allocator-free hot paths); calls
+    that may overlap on the GPU share that array and must be serialised."""
+    import torch
+    _check_keys(keys, num_bins)
+    out = _out_bins(keys, num_bins, out)
+    with torch.cuda.device(keys.device):
+        _check(lib().dsmem_hist_static(keys.data_ptr(), keys.numel(), int(num_bins),
+                                       out.data_ptr(), _stream_handle(stream)))
     return out
 
 

@@ -431,6 +431,48 @@ int run_host(const int32_t* h_keys, int64_t n, int32_t num_bins, uint32_t* h_bin
 }
 
 }  // namespace
+
+// For the entry point with caller-free scratch (static_scratch.cu): the same
+// argument checks, plan and launches as dsmem_hist, with the partial rows in
+// memory the caller of this function supplies, at most `max_rows_bytes`.
+int run_with_fixed_scratch(const int32_t* keys, int64_t n, int32_t num_bins, uint32_t* bins,
+                           uint32_t* scratch, int64_t max_rows_bytes, cudaStream_t stream) {
+  int rc = check_args(keys, n, num_bins, bins);
+  if (rc) return rc;
+  const int64_t row_bytes = 4 * ((static_cast<int64_t>(num_bins) + 3) & ~int64_t{3});
+  if (row_bytes > max_rows_bytes)
+    return fail(DSMEM_HIST_EINVAL,
+                "num_bins %d needs %lld bytes of static scratch per cluster; the static scratch "
+                "holds %lld bytes (at most %lld bins)",
+                num_bins, static_cast<long long>(row_bytes), static_cast<long long>(max_rows_bytes),
+                static_cast<long long>(max_rows_bytes / 4));
+  dsmem_hist_plan_t plan;
+  {
+    std::lock_guard<std::mutex> g(g_mutex);
+    DeviceState* st = nullptr;
+    if ((rc = device_state(&st))) return rc;
+    if ((rc = plan_locked(st, num_bins, n, nullptr, &plan))) return rc;
+    if (plan.workspace_bytes > max_rows_bytes) {
+      // Fewer clusters, so their partial rows fit the static scratch.
+      dsmem_hist_request_t req = {0, 0, static_cast<int32_t>(max_rows_bytes / row_bytes), -1, 0, -1};
+      if ((rc = plan_locked(st, num_bins, n, &req, &plan))) return rc;
+    }
+  }
+  cudaError_t e;
+  if (n == 0) {
+    e = cudaMemsetAsync(bins, 0, sizeof(uint32_t) * static_cast<size_t>(num_bins), stream);
+    return e == cudaSuccess ? DSMEM_HIST_OK : fail_cuda(e, "cudaMemsetAsync");
+  }
+  const ClusterHistArgs args = make_args(plan, keys, n, num_bins, scratch, 0);
+  e = launch_plan(plan, args, stream);
+  if (e == cudaSuccess)
+    e = launch_reduce_partials(scratch, args.stride, static_cast<uint32_t>(plan.num_clusters),
+                               args.num_bins, bins, stream);
+  return e == cudaSuccess ? DSMEM_HIST_OK : fail_cuda(e, "cluster histogram launch");
+}
+
+int record_error(int code, const char* what) { return fail(code, "%s", what); }
+
 }  // namespace dsmh
 
 using namespace dsmh;

@@ -63,6 +63,13 @@ cudaError_t prepare_cluster_kernel(int aggregate, int smem_bytes);
 cudaError_t query_max_active_clusters(int aggregate, int cluster_size, int block_threads,
                                       int smem_bytes, int* out);
 
+// The whole histogram with partial rows in caller-supplied device memory of
+// at most max_rows_bytes (api.cpp; used by static_scratch.cu).
+int run_with_fixed_scratch(const int32_t* keys, int64_t n, int32_t num_bins, uint32_t* bins,
+                           uint32_t* scratch, int64_t max_rows_bytes, cudaStream_t stream);
+// Records a message for dsmem_hist_last_error and returns `code`.
+int record_error(int code, const char* what);
+
 // Planner (pure host logic, planner.cpp).
 int plan_shape(const dsmem_hist_device_t* dev, int32_t num_bins, int64_t n,
                const dsmem_hist_request_t* req, int32_t max_active_clusters,

@@ -165,6 +165,26 @@ DSMEM_HIST_API int dsmem_hist_reduce(const uint32_t* partials, int32_t num_clust
                                      int64_t partial_stride, int32_t num_bins, uint32_t* bins,
                                      cudaStream_t stream);
 
+/* Same result as dsmem_hist, but the library allocates nothing.  The pages
+ * have no counterpart: this is for callers that cannot let a library
+ * allocate device memory -- code running while a stream is captured into a
+ * CUDA graph, applications that own all device memory through their own
+ * arena or budget, and latency-critical paths that must not enter the
+ * allocator (which can synchronise or block).
+ *   keys, n, bins, stream   as for dsmem_hist (device pointers, asynchronous)
+ *   num_bins                1 .. 8,388,608; larger values return EINVAL
+ * The per-cluster partial histograms live in a fixed 32 MiB
+ * `static __device__` array inside the library, held by every GPU that loads
+ * the library until the process exits; fewer clusters are launched when
+ * their rows would not fit.  The first call on a device looks up that
+ * array's device address and prepares the kernels and the plan cache; make
+ * that first call before any stream capture.  The array is overwritten by
+ * every call (nothing in it needs clearing), and all calls share it: calls
+ * that may overlap on the GPU (different streams without ordering, or
+ * different host threads) race on it and must be serialised by the caller. */
+DSMEM_HIST_API int dsmem_hist_static(const int32_t* keys, int64_t n, int32_t num_bins,
+                                     uint32_t* bins, cudaStream_t stream);
+
 /* Plan for the current device (queries its properties and the occupancy of
  * the chosen shape).  `request` may be NULL. */
 DSMEM_HIST_API int dsmem_hist_plan(int32_t num_bins, int64_t n, const dsmem_hist_request_t* request,
