@@ -45,7 +45,12 @@ FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 L2_BYTES = 129 * 1024 * 1024
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "cluster_hist_traffic.json")
-KERNEL_SOURCE = os.path.join(ROOT, "cluster_distributed_shared_gb300", "csrc", "cluster_hist.cu")
+KERNEL_SOURCES = {  # plan kernel id -> (kernel name, source file)
+    0: ("cluster_hist_kernel", os.path.join(ROOT, "cluster_distributed_shared_gb300", "csrc",
+                                            "cluster_hist.cu")),
+    1: ("cluster_ship_kernel", os.path.join(ROOT, "cluster_distributed_shared_gb300", "csrc",
+                                            "cluster_ship.cu")),
+}
 
 
 def parse():
@@ -177,16 +182,19 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_traffic(n_keys, num_bins, cluster_size):
+def kernel_traffic(n_keys, num_bins, cluster_size, kernel_id):
     """Per-launch DRAM bytes of the cluster kernel from the committed ncu
     summary, scaled to this launch's keys; None when the kernel source has
     changed since the counters were taken."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
-        with open(KERNEL_SOURCE, "rb") as f:
+        name, source = KERNEL_SOURCES[kernel_id]
+        with open(source, "rb") as f:
             sha = hashlib.sha256(f.read()).hexdigest()
-    except (OSError, ValueError):
+        if not rec.get("kernel", "").startswith(name):
+            return None
+    except (OSError, ValueError, KeyError):
         return None
     if rec.get("kernel_source_sha256") != sha:
         return None
@@ -366,7 +374,7 @@ def run_ours(a, world, rank, local):
     peak, peak_src = hbm_peak()
     alg_bytes = 4 * n + 4 * num_bins
     achieved = alg_bytes / (cluster_ms / 1e3) / 1e9
-    traffic = kernel_traffic(n, num_bins, P)
+    traffic = kernel_traffic(n, num_bins, P, plan["kernel"])
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -375,7 +383,7 @@ def run_ours(a, world, rank, local):
         "plan": plan,
         "achieved_gbs": world * alg_bytes / (ms_step / 1e3) / 1e9,
         "pct_of_nominal_8tbs": 100.0 * (alg_bytes / (ms_step / 1e3) / 1e9) / NOMINAL_HBM_GBS,
-        "roofline": {"bound": "hbm", "kernel": "cluster_hist_kernel", "achieved": achieved,
+        "roofline": {"bound": "hbm", "kernel": KERNEL_SOURCES[plan["kernel"]][0], "achieved": achieved,
                      "peak": peak, "peak_source": peak_src, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes": alg_bytes, "avg_launch_ms": cluster_ms,
