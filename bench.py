@@ -204,6 +204,29 @@ def kernel_traffic(n_keys, num_bins, cluster_size, kernel_id):
     return None
 
 
+# ---------------------------------------------------------------- multi-rank
+
+def replica_seed(seed, rank):
+    """Each rank histograms its own independent replica of the workload."""
+    return seed + rank
+
+
+def max_over_ranks(x, dist=None, device=None):
+    """The slowest rank's value (time), via one MAX all-reduce; the rank's
+    own value when running alone."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, n, steps, ms_total):
+    """Keys per second over all ranks: every rank processed n keys per step."""
+    return world * n * steps / (ms_total / 1e3)
+
+
 # ---------------------------------------------------------------- reference arm
 
 def run_reference(a, world, rank):
@@ -265,7 +288,7 @@ def run_ours(a, world, rank, local):
         pg = dist
 
     cfg = workload_config(a.workload, a.seed)
-    seed = a.seed + rank
+    seed = replica_seed(a.seed, rank)
     n, num_bins, P = cfg["n"], cfg["num_bins"], cfg["cluster_size"]
     keys_h = gen.workload(a.workload, seed)
     keys = torch.from_numpy(keys_h).to(dev)
@@ -324,12 +347,9 @@ def run_ours(a, world, rank, local):
     ms_total = ev_start.elapsed_time(ev_end)
     kernel_ms = [s.elapsed_time(e) for s, e in ev_k]
     cluster_ms = sum(kernel_ms) / len(kernel_ms)
-    if pg:
-        t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, pg, dev)
     ms_step = ms_total / a.steps
-    value = world * n * a.steps / (ms_total / 1e3)
+    value = whole_job_rate(world, n, a.steps, ms_total)
 
     # The global-atomics comparison kernel, timed the same way on the same keys.
     cmp_steps = max(1, min(a.steps, 50))
@@ -359,11 +379,7 @@ def run_ours(a, world, rank, local):
         t0 = time.perf_counter()
         for _ in range(e2e_steps):
             pkg.dsmem_hist_host(keys_pin, num_bins, out=out_pin)
-        dt = time.perf_counter() - t0
-        if pg:
-            t = torch.tensor([dt], dtype=torch.float64, device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            dt = float(t.item())
+        dt = max_over_ranks(time.perf_counter() - t0, pg, dev)
         ok = parity is None or np.array_equal(out_pin.numpy().view(np.uint32), want)
         e2e = {"value": world * n * e2e_steps / dt, "unit": UNIT,
                "h2d_bytes_per_step": 4 * n, "d2h_bytes_per_step": 4 * num_bins,

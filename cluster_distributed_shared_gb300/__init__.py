@@ -59,6 +59,15 @@ class Plan(ctypes.Structure):
         return {name: getattr(self, name) for name, _ in self._fields_}
 
 
+class TuneResult(ctypes.Structure):
+    _fields_ = [
+        ("plan", Plan),
+        ("global_atomic", ctypes.c_int32),
+        ("ms", ctypes.c_float),
+        ("control_ms", ctypes.c_float),
+    ]
+
+
 class Request(ctypes.Structure):
     _fields_ = [
         ("cluster_size", ctypes.c_int32),
@@ -84,7 +93,8 @@ class Device(ctypes.Structure):
 
 EXPORTS = (
     "dsmem_hist", "dsmem_hist_ex", "dsmem_hist_global_atomic", "dsmem_hist_host",
-    "dsmem_hist_partials", "dsmem_hist_reduce", "dsmem_hist_static",
+    "dsmem_hist_partials", "dsmem_hist_reduce", "dsmem_hist_static", "dsmem_hist_tune",
+    "dsmem_hist_microbench",
     "dsmem_hist_plan", "dsmem_hist_plan_for_device", "dsmem_hist_strerror",
     "dsmem_hist_last_error", "dsmem_hist_release", "dsmem_hist_version",
 )
@@ -111,6 +121,10 @@ def lib():
                 ("dsmem_hist_ex", [p, i64, i32, p, ctypes.POINTER(Request), p]),
                 ("dsmem_hist_global_atomic", [p, i64, i32, p, p]),
                 ("dsmem_hist_static", [p, i64, i32, p, p]),
+                ("dsmem_hist_microbench", [i32, i32, i32, ctypes.POINTER(ctypes.c_double),
+                                           ctypes.POINTER(ctypes.c_double)]),
+                ("dsmem_hist_tune", [p, i64, i32, i64, i32, ctypes.POINTER(TuneResult),
+                                     ctypes.POINTER(i32), p]),
                 ("dsmem_hist_host", [p, i64, i32, p, p]),
                 ("dsmem_hist_partials", [p, i64, i32, ctypes.POINTER(Plan), p, i32, p]),
                 ("dsmem_hist_reduce", [p, i32, i64, i32, p, p]),
@@ -301,6 +315,46 @@ def dsmem_hist_reduce(partials, num_clusters: int, partial_stride: int, num_bins
     with torch.cuda.device(partials.device):
         _check(lib().dsmem_hist_reduce(partials.data_ptr(), int(num_clusters), int(partial_stride),
                                        int(num_bins), out.data_ptr(), _stream_handle(stream)))
+    return out
+
+
+MICROBENCH_KINDS = {
+    "local_red": 0,
+    "remote_red": 1,
+    "remote_st16_scattered": 2,
+    "remote_st16_coalesced": 3,
+    "cluster_barrier": 4,
+}
+
+
+def dsmem_hist_microbench(kind: str, cluster_size: int, iters: int = 4096) -> dict:
+    """One DSMEM primitive's rate on the current GPU (see the C header):
+    ops (or bytes) per clock per SM, or cycles per cluster barrier."""
+    value, ms = ctypes.c_double(0), ctypes.c_double(0)
+    _check(lib().dsmem_hist_microbench(MICROBENCH_KINDS[kind], int(cluster_size), int(iters),
+                                       ctypes.byref(value), ctypes.byref(ms)))
+    unit = {"cluster_barrier": "cycles/barrier", "remote_st16_scattered": "bytes/clk/SM",
+            "remote_st16_coalesced": "bytes/clk/SM"}.get(kind, "ops/clk/SM")
+    return {"kind": kind, "cluster_size": cluster_size, "value": value.value, "unit": unit,
+            "ms": ms.value}
+
+
+def dsmem_hist_tune(keys, num_bins: int, sample_keys: int = 0, stream=None) -> list:
+    """Times every legal cluster shape (and the global-atomics kernel) on a
+    sample of `keys`; returns dicts sorted fastest first: plan fields plus
+    `global_atomic`, `ms` and `control_ms`.  Synchronous."""
+    import torch
+    _check_keys(keys, num_bins)
+    res = (TuneResult * 16)()
+    count = ctypes.c_int32(0)
+    with torch.cuda.device(keys.device):
+        _check(lib().dsmem_hist_tune(keys.data_ptr(), keys.numel(), int(num_bins), int(sample_keys),
+                                     16, res, ctypes.byref(count), _stream_handle(stream)))
+    out = []
+    for r in res[: count.value]:
+        d = r.plan.as_dict()
+        d.update(global_atomic=r.global_atomic, ms=r.ms, control_ms=r.control_ms)
+        out.append(d)
     return out
 
 

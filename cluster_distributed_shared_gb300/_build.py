@@ -15,7 +15,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libdsmemhist.so")
 
-SOURCES = ["cluster_hist.cu", "cluster_ship.cu", "static_scratch.cu", "planner.cpp", "api.cpp"]
+SOURCES = ["cluster_hist.cu", "cluster_ship.cu", "static_scratch.cu", "microbench.cu", "planner.cpp",
+           "api.cpp"]
 HEADERS = [os.path.join(CSRC, "internal.h"), os.path.join(CSRC, "ptx.cuh"),
            os.path.join(INCLUDE, "dsmem_hist.h")]
 

@@ -8,8 +8,11 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
 #include <map>
 #include <mutex>
+#include <utility>
+#include <vector>
 #include <string>
 #include <tuple>
 
@@ -473,6 +476,131 @@ int run_with_fixed_scratch(const int32_t* keys, int64_t n, int32_t num_bins, uin
 
 int record_error(int code, const char* what) { return fail(code, "%s", what); }
 
+namespace {
+
+// Median of the elapsed times of `reps` launches of `fn`, each bracketed by
+// its own pair of events on `stream`.
+template <class Fn>
+int time_median(Fn fn, cudaStream_t stream, int reps, float* out) {
+  cudaEvent_t a = nullptr, b = nullptr;
+  cudaError_t e;
+  if ((e = cudaEventCreate(&a)) != cudaSuccess || (e = cudaEventCreate(&b)) != cudaSuccess) {
+    if (a) cudaEventDestroy(a);
+    return fail_cuda(e, "cudaEventCreate");
+  }
+  float t[16];
+  int rc = DSMEM_HIST_OK;
+  if ((rc = fn()) != DSMEM_HIST_OK) goto done;  // warm-up
+  for (int i = 0; i < reps && i < 16; ++i) {
+    cudaEventRecord(a, stream);
+    if ((rc = fn()) != DSMEM_HIST_OK) goto done;
+    cudaEventRecord(b, stream);
+    if ((e = cudaEventSynchronize(b)) != cudaSuccess) {
+      rc = fail_cuda(e, "cudaEventSynchronize");
+      goto done;
+    }
+    cudaEventElapsedTime(&t[i], a, b);
+  }
+  for (int i = 1; i < reps; ++i)
+    for (int j = i; j > 0 && t[j] < t[j - 1]; --j) std::swap(t[j], t[j - 1]);
+  *out = t[reps / 2];
+done:
+  cudaEventDestroy(a);
+  cudaEventDestroy(b);
+  return rc;
+}
+
+}  // namespace
+
+int run_tune(const int32_t* keys, int64_t n, int32_t num_bins, int64_t sample_keys,
+             int32_t max_results, dsmem_hist_tune_result_t* results, int32_t* num_results,
+             cudaStream_t stream) {
+  int rc = check_args(keys, n, num_bins, keys);
+  if (rc) return rc;
+  if (!results || !num_results || max_results < 1)
+    return fail(DSMEM_HIST_EINVAL, "results, num_results and max_results >= 1 are required");
+  const int64_t m = std::min<int64_t>(n, sample_keys > 0 ? sample_keys : (int64_t{1} << 24));
+  DeviceState* st = nullptr;
+  {
+    std::lock_guard<std::mutex> g(g_mutex);
+    if ((rc = device_state(&st))) return rc;
+    if ((rc = ensure_pool(st))) return rc;
+  }
+  // Candidates: every cluster size with each kernel, duplicates of one shape
+  // removed, then the global-atomics kernel.
+  std::vector<dsmem_hist_tune_result_t> cand;
+  const int sizes[] = {1, 2, 4, 8, 16};
+  for (int P : sizes) {
+    for (int k = DSMEM_HIST_KERNEL_DIRECT; k <= DSMEM_HIST_KERNEL_SHIP; ++k) {
+      dsmem_hist_request_t req = {P, 0, 0, 0, 0, k};
+      dsmem_hist_plan_t plan;
+      {
+        std::lock_guard<std::mutex> g(g_mutex);
+        if (plan_locked(st, num_bins, m, &req, &plan) != DSMEM_HIST_OK) continue;
+      }
+      bool dup = false;
+      for (const auto& c : cand)
+        dup |= c.plan.cluster_size == plan.cluster_size && c.plan.kernel == plan.kernel;
+      if (dup) continue;
+      dsmem_hist_tune_result_t r = {};
+      r.plan = plan;
+      cand.push_back(r);
+    }
+  }
+  dsmem_hist_tune_result_t ga = {};
+  ga.global_atomic = 1;
+  cand.push_back(ga);
+  g_last_error.clear();
+
+  int64_t ws = 0;
+  for (const auto& c : cand) ws = std::max(ws, c.plan.workspace_bytes);
+  const size_t bins_bytes = (4 * static_cast<size_t>(num_bins) + 255) & ~size_t{255};
+  void* scratch = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&scratch, bins_bytes + static_cast<size_t>(ws) + 256,
+                                          st->pool, stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(DSMEM_HIST_ENOMEM, "tune scratch: %s", cudaGetErrorString(e));
+  }
+  uint32_t* d_bins = static_cast<uint32_t*>(scratch);
+  uint32_t* partials = reinterpret_cast<uint32_t*>(static_cast<char*>(scratch) + bins_bytes);
+  uint32_t* sink = reinterpret_cast<uint32_t*>(static_cast<char*>(scratch) + bins_bytes + ws);
+  for (auto& c : cand) {
+    if (c.global_atomic) {
+      rc = time_median([&] {
+        const cudaError_t le = launch_global_atomic(keys, m, static_cast<uint32_t>(num_bins), d_bins, stream);
+        return le == cudaSuccess ? DSMEM_HIST_OK : fail_cuda(le, "global-atomic launch");
+      }, stream, 5, &c.ms);
+      if (rc) break;
+      continue;
+    }
+    const dsmem_hist_plan_t plan = c.plan;
+    rc = time_median([&] {
+      const ClusterHistArgs args = make_args(plan, keys, m, num_bins, partials, 0);
+      cudaError_t le = launch_plan(plan, args, stream);
+      if (le == cudaSuccess)
+        le = launch_reduce_partials(partials, args.stride, static_cast<uint32_t>(plan.num_clusters),
+                                    args.num_bins, d_bins, stream);
+      return le == cudaSuccess ? DSMEM_HIST_OK : fail_cuda(le, "tune launch");
+    }, stream, 5, &c.ms);
+    if (rc) break;
+    rc = time_median([&] {
+      const cudaError_t le = launch_cluster_control(plan, sink, stream);
+      return le == cudaSuccess ? DSMEM_HIST_OK : fail_cuda(le, "control launch");
+    }, stream, 5, &c.control_ms);
+    if (rc) break;
+  }
+  cudaFreeAsync(scratch, stream);
+  cudaStreamSynchronize(stream);
+  if (rc) return rc;
+  std::sort(cand.begin(), cand.end(),
+            [](const dsmem_hist_tune_result_t& x, const dsmem_hist_tune_result_t& y) { return x.ms < y.ms; });
+  const int32_t k = std::min<int32_t>(max_results, static_cast<int32_t>(cand.size()));
+  for (int32_t i = 0; i < k; ++i) results[i] = cand[i];
+  *num_results = k;
+  return DSMEM_HIST_OK;
+}
+
 }  // namespace dsmh
 
 using namespace dsmh;
@@ -500,6 +628,12 @@ int dsmem_hist_global_atomic(const int32_t* keys, int64_t n, int32_t num_bins, u
 int dsmem_hist_host(const int32_t* h_keys, int64_t n, int32_t num_bins, uint32_t* h_bins,
                     cudaStream_t stream) {
   return run_host(h_keys, n, num_bins, h_bins, stream);
+}
+
+int dsmem_hist_tune(const int32_t* keys, int64_t n, int32_t num_bins, int64_t sample_keys,
+                    int32_t max_results, dsmem_hist_tune_result_t* results, int32_t* num_results,
+                    cudaStream_t stream) {
+  return run_tune(keys, n, num_bins, sample_keys, max_results, results, num_results, stream);
 }
 
 int dsmem_hist_partials(const int32_t* keys, int64_t n, int32_t num_bins,

@@ -235,6 +235,19 @@ __global__ void __launch_bounds__(512) global_atomic_hist_kernel(const int32_t* 
   }
 }
 
+// Work-free control ("CREDIT", section on the profitability model): the same
+// grid, cluster shape and dynamic shared memory as a cluster histogram
+// launch, zeroing its slice and passing the two cluster barriers, but
+// streaming no keys.  Its time is the launch, residency and synchronisation
+// cost a cluster shape pays before doing any work.
+__global__ void __launch_bounds__(1024, 1) cluster_control_kernel(uint32_t S, uint32_t* sink) {
+  extern __shared__ __align__(16) uint32_t slice[];
+  for (uint32_t i = threadIdx.x; i < S; i += blockDim.x) slice[i] = 0;
+  cluster_barrier();
+  cluster_barrier();
+  if (threadIdx.x == 0 && slice[0] != 0) sink[0] = slice[0];
+}
+
 template <bool kAggregate>
 void* cluster_kernel_ptr() {
   return reinterpret_cast<void*>(&cluster_hist_kernel<kAggregate>);
@@ -251,6 +264,30 @@ cudaError_t prepare_cluster_kernel(int aggregate, int smem_bytes) {
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+}
+
+cudaError_t launch_cluster_control(const dsmem_hist_plan_t& plan, uint32_t* sink,
+                                   cudaStream_t stream) {
+  const void* fn = reinterpret_cast<const void*>(&cluster_control_kernel);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       plan.smem_bytes);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
+    return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(plan.num_clusters) * plan.cluster_size, 1, 1);
+  cfg.blockDim = dim3(plan.block_threads, 1, 1);
+  cfg.dynamicSmemBytes = plan.smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = plan.cluster_size;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, cluster_control_kernel, static_cast<uint32_t>(plan.bins_per_cta),
+                            sink);
 }
 
 cudaError_t query_max_active_clusters(int aggregate, int cluster_size, int block_threads,

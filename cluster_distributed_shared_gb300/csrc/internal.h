@@ -47,6 +47,9 @@ cudaError_t launch_reduce_partials(const uint32_t* partials, uint64_t stride,
                                    cudaStream_t stream);
 cudaError_t launch_global_atomic(const int32_t* keys, int64_t n, uint32_t num_bins,
                                  uint32_t* bins, cudaStream_t stream);
+// Work-free control kernel with a plan's grid, cluster and shared memory.
+cudaError_t launch_cluster_control(const dsmem_hist_plan_t& plan, uint32_t* sink,
+                                   cudaStream_t stream);
 
 // Ship kernel (cluster_ship.cu; its staging size is computed by the planner).
 uint32_t ship_staging_bytes(int cluster_size, int sub_vectors);

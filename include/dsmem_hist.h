@@ -185,6 +185,51 @@ DSMEM_HIST_API int dsmem_hist_reduce(const uint32_t* partials, int32_t num_clust
 DSMEM_HIST_API int dsmem_hist_static(const int32_t* keys, int64_t n, int32_t num_bins,
                                      uint32_t* bins, cudaStream_t stream);
 
+/* One candidate timed by dsmem_hist_tune. */
+typedef struct dsmem_hist_tune_result {
+  dsmem_hist_plan_t plan;  /* the shape (meaningless when global_atomic == 1) */
+  int32_t global_atomic;   /* 1: the global-atomics kernel, no cluster */
+  float ms;                /* median time of the whole histogram (cluster kernel + reduction) */
+  float control_ms;        /* median time of the work-free control launch of this shape */
+} dsmem_hist_tune_result_t;
+
+/* Cluster-shape screen ("CREDIT", sections on the profitability model and
+ * the matched control kernel): times every legal shape for this num_bins --
+ * cluster sizes 1, 2, 4, 8, 16 with the direct and the ship kernel -- and
+ * the global-atomics kernel on the first min(n, sample_keys) keys
+ * (sample_keys <= 0: 16,777,216), each as the median of 5 timed runs after a
+ * warm-up, together with a work-free control launch of the same grid,
+ * cluster and shared memory.  Writes up to max_results results sorted by
+ * `ms` (fastest first) and their count; the fastest plan can be passed back
+ * through dsmem_hist_ex (cluster_size, block_threads, kernel, aggregate).
+ * SYNCHRONOUS on `stream`; uses scratch from the library's pool and writes
+ * nothing the caller owns. */
+DSMEM_HIST_API int dsmem_hist_tune(const int32_t* keys, int64_t n, int32_t num_bins,
+                                   int64_t sample_keys, int32_t max_results,
+                                   dsmem_hist_tune_result_t* results, int32_t* num_results,
+                                   cudaStream_t stream);
+
+/* DSMEM primitive microbenchmarks (kinds for dsmem_hist_microbench). */
+enum {
+  DSMEM_HIST_MB_LOCAL_RED = 0,             /* red.shared.add.u32, random counter of own slice */
+  DSMEM_HIST_MB_REMOTE_RED = 1,            /* red.shared::cluster.add.u32 into a peer's slice */
+  DSMEM_HIST_MB_REMOTE_ST16_SCATTERED = 2, /* st.shared::cluster.v4, random peer and address */
+  DSMEM_HIST_MB_REMOTE_ST16_COALESCED = 3, /* st.shared::cluster.v4, 512 contiguous bytes per warp */
+  DSMEM_HIST_MB_CLUSTER_BARRIER = 4        /* barrier.cluster arrive + wait */
+};
+
+/* Measures one DSMEM primitive on the current GPU ("Hopper DSMEM vs HBM",
+ * tile-exchange and ping-pong sections; "CREDIT", microbenchmark section):
+ * 1024 threads per CTA, 128 KiB of shared memory per CTA, every resident
+ * cluster of `cluster_size` CTAs, `iters` operations per thread.
+ *   *value  operations per clock per SM (bytes per clock per SM for the two
+ *           store kinds; clock cycles per barrier for the barrier kind)
+ *   *ms     wall time of the timed launch
+ * Synchronous; allocates and frees its own small device buffers.  With
+ * cluster_size 1 the "remote" kinds address this CTA itself. */
+DSMEM_HIST_API int dsmem_hist_microbench(int32_t kind, int32_t cluster_size, int32_t iters,
+                                         double* value, double* ms);
+
 /* Plan for the current device (queries its properties and the occupancy of
  * the chosen shape).  `request` may be NULL. */
 DSMEM_HIST_API int dsmem_hist_plan(int32_t num_bins, int64_t n, const dsmem_hist_request_t* request,

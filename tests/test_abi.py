@@ -197,3 +197,16 @@ def test_aggregate_and_kernel_overrides():
         with pytest.raises(pkg.DsmemHistError) as e:
             plan(GB300, 4096, 1 << 20, **bad)
         assert e.value.code == pkg.DSMEM_HIST_EINVAL
+
+
+def test_tune_and_microbench_reject_bad_arguments():
+    L = pkg.lib()
+    buf = (ctypes.c_uint32 * 8)()
+    p = ctypes.cast(buf, ctypes.c_void_p)
+    count = ctypes.c_int32(0)
+    res = (pkg.TuneResult * 2)()
+    assert L.dsmem_hist_tune(p, -1, 8, 0, 2, res, ctypes.byref(count), None) == pkg.DSMEM_HIST_EINVAL
+    assert L.dsmem_hist_tune(p, 4, 0, 0, 2, res, ctypes.byref(count), None) == pkg.DSMEM_HIST_EINVAL
+    v, ms = ctypes.c_double(), ctypes.c_double()
+    assert L.dsmem_hist_microbench(0, 17, 16, ctypes.byref(v), ctypes.byref(ms)) == pkg.DSMEM_HIST_EINVAL
+    assert L.dsmem_hist_microbench(0, 2, 0, ctypes.byref(v), ctypes.byref(ms)) == pkg.DSMEM_HIST_EINVAL
