@@ -65,6 +65,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cluster", type=int, default=0,
+                    help="cluster size (default: the workload's published one)")
     a = ap.parse_args()
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -289,6 +291,8 @@ def run_ours(a, world, rank, local):
 
     cfg = workload_config(a.workload, a.seed)
     seed = replica_seed(a.seed, rank)
+    if a.cluster:
+        cfg["cluster_size"] = a.cluster
     n, num_bins, P = cfg["n"], cfg["num_bins"], cfg["cluster_size"]
     keys_h = gen.workload(a.workload, seed)
     keys = torch.from_numpy(keys_h).to(dev)

@@ -28,6 +28,7 @@ DSMEM_HIST_ENOMEM = -5
 
 KERNEL_DIRECT = 0
 KERNEL_SHIP = 1
+SHIP_THREADS = 768  # DSMEM_HIST_SHIP_THREADS
 
 
 class DsmemHistError(RuntimeError):
@@ -96,7 +97,8 @@ EXPORTS = (
     "dsmem_hist_partials", "dsmem_hist_reduce", "dsmem_hist_static", "dsmem_hist_tune",
     "dsmem_hist_microbench",
     "dsmem_hist_plan", "dsmem_hist_plan_for_device", "dsmem_hist_strerror",
-    "dsmem_hist_last_error", "dsmem_hist_release", "dsmem_hist_version",
+    "dsmem_hist_last_error", "dsmem_hist_release", "dsmem_hist_device_status",
+    "dsmem_hist_version",
 )
 
 _lib = None
@@ -142,6 +144,8 @@ def lib():
             L.dsmem_hist_last_error.restype = ctypes.c_char_p
             L.dsmem_hist_release.argtypes = []
             L.dsmem_hist_release.restype = None
+            L.dsmem_hist_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+            L.dsmem_hist_device_status.restype = ctypes.c_int
             L.dsmem_hist_version.argtypes = []
             L.dsmem_hist_version.restype = ctypes.c_int
             _lib = L
@@ -380,6 +384,16 @@ def dsmem_hist_plan_for_device(device: dict, num_bins: int, n: int, max_active_c
 
 def dsmem_hist_release() -> None:
     lib().dsmem_hist_release()
+
+
+def dsmem_hist_device_status() -> int:
+    """Reads and clears the ship kernel's device status word (0: every
+    bounded inbox wait succeeded since the last call)."""
+    word = ctypes.c_uint32(0)
+    rc = lib().dsmem_hist_device_status(ctypes.byref(word))
+    if rc not in (DSMEM_HIST_OK, DSMEM_HIST_ETIMEOUT):
+        _check(rc)
+    return word.value
 
 
 def dsmem_hist_version() -> int:

@@ -289,7 +289,7 @@ int check_plan(const DeviceState* st, const dsmem_hist_plan_t* p, int32_t num_bi
     return fail(DSMEM_HIST_EINVAL, "plan: cluster_size %lld out of range", static_cast<long long>(P));
   if (p->kernel == DSMEM_HIST_KERNEL_SHIP) {
     const int nq = p->sub_vectors;
-    if (P < 2 || p->block_threads != 1024 || (p->keys_per_thread != 4 && p->keys_per_thread != 8) ||
+    if (P < 2 || p->block_threads != kShipThreads || (p->keys_per_thread != 4 && p->keys_per_thread != 8) ||
         nq < 1 || nq > 32 || S + 32 >= 0xFFFF ||
         p->smem_bytes != 4 * S + static_cast<int64_t>(ship_staging_bytes(static_cast<int>(P), nq)))
       return fail(DSMEM_HIST_EINVAL, "plan: ship kernel fields inconsistent");
@@ -703,6 +703,15 @@ void dsmem_hist_release(void) {
     }
   }
   if (have_cur) cudaSetDevice(cur);
+}
+
+int dsmem_hist_device_status(uint32_t* status) {
+  uint32_t word = 0;
+  const cudaError_t e = read_and_clear_ship_status(&word);
+  if (status) *status = word;
+  if (e != cudaSuccess) return fail(DSMEM_HIST_ECUDA, "device_status: %s", cudaGetErrorString(e));
+  if (word) return fail(DSMEM_HIST_ETIMEOUT, "device_status: a bounded inbox wait gave up (word 0x%x)", word);
+  return DSMEM_HIST_OK;
 }
 
 int dsmem_hist_version(void) { return 100; }

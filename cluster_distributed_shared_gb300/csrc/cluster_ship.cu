@@ -9,37 +9,45 @@
 // remote `red.shared::cluster` sustains ~0.33 operations per clock per SM
 // while a local shared-memory atomic sustains ~12, and coalesced 16-byte
 // remote stores move ~19 bytes per clock per SM.  So each key travels as a
-// 16-bit local index inside 16-byte vectors, and its owner applies a local
-// `red.shared` (the "push compact data to its owner, combine locally" idea of
-// "CREDIT", section on the clustered reduction-reuse schedule).
+// 16-bit local index inside contiguous 16-byte vectors, and its owner applies
+// a local `red.shared` (the "push compact data to its owner, combine locally"
+// idea of "CREDIT", section on the clustered reduction-reuse schedule).
 //
-// Per CTA (1024 threads, 32 warps), keys are processed in rounds of
-// 1024 * kKpt keys.
-//   A  partition (all warps): sub-bucket (owner o, lane L) is a contiguous
-//      run of qs 16-bit entries; consecutive sub-buckets are 2*qs + 4 bytes
-//      apart, a 4-byte skew that puts lane L's next entry in bank
-//      (L + fill/2) mod 32, so a warp's 32 stores spread over the banks.  Its
-//      cursor holds the shared-memory byte address of its next entry, so one
-//      local `atom.add 2` both reserves the slot and yields the store address;
-//      the 32 lanes of a warp touch 32 different cursors (one bank each).  A
-//      key whose sub-bucket is full goes to its owner with a remote red
-//      (exact, slow, only on skewed rounds).  A warp tile of 128 equal keys
-//      is counted with one red of 128 (pre-aggregation of runs).
-//   After a CTA barrier:
-//   B  `ns` shipper warps per owner close its 32 sub-buckets (lane = sub-
-//      bucket): pad the last vector with the index of one of 32 dummy
-//      counters after the slice, scan the vector counts, and copy every
-//      vector (four 32-bit shared loads, one st.shared::cluster.v4) into the
-//      owner's inbox slot for this sender, plus one vector count; the CTA's
-//      own keys go to its own inbox the same way.
-//   D  the other warps apply the previous round's inbox (complete since the
-//      last cluster barrier wait) with one local red per entry.
-//   After a CTA barrier, receivers arrive on the cluster barrier (relaxed:
-//   they published no remote writes), every warp partitions the next round,
-//   shippers arrive (release: their inbox stores), and all wait.
+// Per CTA (kShipThreads threads), keys are processed in rounds of
+// kShipThreads * kKpt keys; every warp does every phase.
+//   Partition.  Owner o's staging block is column-major: rows of 64 bytes,
+//     column L (0..31) holding the keys that lane L of any warp routed to o.
+//     Cursor (o, L) is the byte address of the column's next free entry, so
+//     one local `atom.add 64` both reserves the entry and yields the store
+//     address.  The 32 lanes of a warp touch 32 cursors in 32 banks, and
+//     their 16-bit stores fall at most two to a bank.  A key whose column is
+//     full goes to its owner with a remote red (exact, slow, only on skewed
+//     rounds); a key outside the pass's bins meets a cursor row that is
+//     always full and is dropped on the same path.  A warp tile of 128 equal
+//     keys becomes one remote red of 128 (pre-aggregation of runs).
+//   Ship (after a CTA barrier that ends the partition).  Warps serve owner
+//     w mod P: the block's row count is the fullest column's fill, and its
+//     rows go out as contiguous 16-byte `st.async` stores into the owner's
+//     inbox slot for this sender, then are overwritten with padding entries
+//     (column c pads with index S + c, one of 32 never-read counters after
+//     the slice).  The row count goes to the owner's header the same way.
+//     Each store's bytes are counted on the owner's mbarrier for that inbox
+//     buffer, on which every sender arrives once per round with its byte
+//     count (`mbarrier.arrive.expect_tx`).
+//   Apply.  The same warps wait (bounded) for the previous round's mbarrier
+//     phase, then apply that round's inbox block from sender w mod P: one
+//     `dp2a` turns a 16-bit entry into its counter's address, one local red
+//     increments it.
+//   After a CTA barrier, every warp arrives on the cluster barrier, partitions
+//   the next round, and waits.  Since the mbarriers publish the inbox data,
+//   this barrier is relaxed: it only tells senders that the inbox they are
+//   about to overwrite has been read, so no warp waits for its remote stores
+//   to be acknowledged.
 // Inboxes are double-buffered: a sender writes round r into buffer r%2 only
-// after waiting on the barrier of round r-1, which every owner arrives on
-// only after it has applied round r-2 from that buffer.
+// after the barrier of round r-1, which every owner arrives on only after it
+// has applied round r-2 from that buffer.  Cursor sets alternate by round, so
+// the set a round's ship reads is reset while the next round partitions with
+// the other set.
 
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -52,16 +60,24 @@ namespace {
 
 using namespace ptx;
 
+constexpr uint32_t kFullMask = 0xffffffffu;
+// Cursor value of the row that collects keys outside the pass's bins: at or
+// above every block's end for any number of increments in one round.
+constexpr uint32_t kAlwaysFull = 0xFFFF0000u;
+
 struct Ctx {
   uint32_t base, range;   // current pass: first bin, bins in the pass
-  uint32_t S, lgS, P, lane;
-  uint32_t owner_bytes;   // bytes between sub-buckets (o, L) and (o + 1, L): 32*(2*qs + 4)
+  uint32_t S, lgS, P, PS; // PS = P * S
+  uint32_t lane;
   uint64_t magic;
   uint32_t slice;         // shared::cta address of u32[S + 32]
-  uint32_t cursor_lane;   // &cursor[0*32 + lane]
-  uint32_t limit_lane;    // end of sub-bucket (0, lane)
+  uint32_t cur_lane;      // this round's cursor set + 4 * lane
+  uint32_t lim0;          // end of owner 0's staging block
+  uint32_t blk;           // bytes per owner block: 64 * rows
+  uint32_t sink;          // 16-bit store target of keys that are not staged
 };
 
+// Owner and local counter of an in-pass offset `rel` < P*S.
 __device__ __forceinline__ void owner_local(uint32_t rel, const Ctx& c, uint32_t& o,
                                             uint32_t& loc, bool pow2) {
   if (pow2) {
@@ -73,35 +89,13 @@ __device__ __forceinline__ void owner_local(uint32_t rel, const Ctx& c, uint32_t
   }
 }
 
-// One key of A, fused into one predicated PTX block: if `rel < range`,
-// reserve the next slot of sub-bucket (owner, lane) (`atom.add` on its
-// cursor returns the slot's byte address) and, if that address is below the
-// sub-bucket's end, store the 16-bit local index there.  Returns 1 when the key is valid
-// but its sub-bucket is full (the caller increments the owner directly).
-__device__ __forceinline__ uint32_t place_key(uint32_t rel, uint32_t range, uint32_t cursor_addr,
-                                              uint32_t stride, uint32_t limit, uint32_t loc,
-                                              uint32_t& ea) {
-  uint32_t spill;
-  asm volatile(
-      "{\n\t.reg .pred pv, pf, ps;\n\t"
-      "setp.lt.u32 pv, %2, %3;\n\t"
-      "mov.u32 %0, 0;\n\t"
-      "@pv atom.shared.add.u32 %0, [%4], %5;\n\t"
-      "setp.lt.and.u32 pf, %0, %6, pv;\n\t"
-      "setp.ge.and.u32 ps, %0, %6, pv;\n\t"
-      "@pf st.shared.u16 [%0], %7;\n\t"
-      "selp.u32 %1, 1, 0, ps;\n\t}"
-      : "=&r"(ea), "=r"(spill)
-      : "r"(rel), "r"(range), "r"(cursor_addr), "r"(stride), "r"(limit), "h"(static_cast<uint16_t>(loc)));
-  return spill;
-}
-
-// A: partition one warp tile (four keys per lane).
+// Partition one warp tile (four keys per lane).  All four reservations are
+// issued before the first store so their latencies overlap.
 template <bool kPow2>
-__device__ __forceinline__ void partition_vec(const int4& v, const Ctx& c) {
+__device__ __forceinline__ void partition_tile(const int4& v, const Ctx& c) {
   const bool eq4 = (v.x == v.y) & (v.y == v.z) & (v.z == v.w);
-  const int32_t k0 = __shfl_sync(0xffffffffu, v.x, 0);
-  if (__all_sync(0xffffffffu, eq4 & (v.x == k0))) {
+  const int32_t k0 = __shfl_sync(kFullMask, v.x, 0);
+  if (__all_sync(kFullMask, eq4 & (v.x == k0))) {
     const uint32_t rel = static_cast<uint32_t>(k0) - c.base;
     if (c.lane == 0 && rel < c.range) {
       uint32_t o, loc;
@@ -111,46 +105,74 @@ __device__ __forceinline__ void partition_vec(const int4& v, const Ctx& c) {
     return;
   }
   const int32_t keys[4] = {v.x, v.y, v.z, v.w};
-  uint32_t rel[4], own[4], loc[4], ea[4], spill = 0;
+  uint32_t own[4], loc[4], ea[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    rel[k] = static_cast<uint32_t>(keys[k]) - c.base;
-    owner_local(rel[k], c, own[k], loc[k], kPow2);
-    spill |= place_key(rel[k], c.range, c.cursor_lane + 128u * own[k], 2u,
-                       c.limit_lane + c.owner_bytes * own[k], loc[k], ea[k]) << k;
+    // Offsets at or past P*S clamp to owner P, the always-full cursor row.
+    const uint32_t rel = min(static_cast<uint32_t>(keys[k]) - c.base, c.PS);
+    owner_local(rel, c, own[k], loc[k], kPow2);
+    ea[k] = atom_add_local(c.cur_lane + (own[k] << 7), 64u);
   }
-  if (__any_sync(0xffffffffu, spill != 0)) {
+  uint32_t spill = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const bool ok = ea[k] < c.lim0 + own[k] * c.blk;
+    st_shared_u16(ok ? ea[k] : c.sink, static_cast<uint16_t>(loc[k]));
+    spill |= ok ? 0u : (1u << k);
+  }
+  if (__any_sync(kFullMask, spill != 0)) {
 #pragma unroll
     for (int k = 0; k < 4; ++k)
-      if (spill & (1u << k)) red_add_cluster(map_rank(c.slice + 4u * loc[k], own[k]), 1u);
+      if (((spill >> k) & 1u) && static_cast<uint32_t>(keys[k]) - c.base < c.range)
+        red_add_cluster(map_rank(c.slice + 4u * loc[k], own[k]), 1u);
   }
 }
 
-// Applies the 8 entries of one received vector (16-bit local indices; padding
-// entries index the dummy counters after the slice).
+// Applies the 8 entries of one received vector.  dp2a.lo with b = 4 gives
+// slice + 4 * low half, with b = 0x400 slice + 4 * high half.
 __device__ __forceinline__ void apply_vector(uint32_t slice, const uint4& x) {
-  red_add_local(slice + 4u * (x.x & 0xFFFFu), 1u);
-  red_add_local(slice + 4u * (x.x >> 16), 1u);
-  red_add_local(slice + 4u * (x.y & 0xFFFFu), 1u);
-  red_add_local(slice + 4u * (x.y >> 16), 1u);
-  red_add_local(slice + 4u * (x.z & 0xFFFFu), 1u);
-  red_add_local(slice + 4u * (x.z >> 16), 1u);
-  red_add_local(slice + 4u * (x.w & 0xFFFFu), 1u);
-  red_add_local(slice + 4u * (x.w >> 16), 1u);
+  red_add_local(__dp2a_lo(x.x, 4u, slice), 1u);
+  red_add_local(__dp2a_lo(x.x, 0x400u, slice), 1u);
+  red_add_local(__dp2a_lo(x.y, 4u, slice), 1u);
+  red_add_local(__dp2a_lo(x.y, 0x400u, slice), 1u);
+  red_add_local(__dp2a_lo(x.z, 4u, slice), 1u);
+  red_add_local(__dp2a_lo(x.z, 0x400u, slice), 1u);
+  red_add_local(__dp2a_lo(x.w, 4u, slice), 1u);
+  red_add_local(__dp2a_lo(x.w, 0x400u, slice), 1u);
+}
+
+__device__ uint32_t g_ship_status;  // bit 0: a bounded wait gave up
+
+// Waits for phase `parity` of an inbox mbarrier, at most ~1e8 cycles
+// (~50 ms).  On a timeout the device status word records it and the caller
+// skips the buffer; once any wait has timed out, later waits give up after
+// one probe.
+__device__ __forceinline__ bool wait_inbox(uint32_t mbar, uint32_t parity) {
+  if (mbar_try_wait(mbar, parity)) return true;
+  if (*reinterpret_cast<volatile uint32_t*>(&g_ship_status) != 0u) return false;
+  const long long deadline = clock64() + 100000000ll;
+  while (clock64() < deadline)
+    if (mbar_try_wait(mbar, parity)) return true;
+  atomicOr(&g_ship_status, 1u);
+  return false;
+}
+
+__device__ __forceinline__ uint4 pad_vector(uint32_t pad0) {
+  return make_uint4(pad0, pad0 + 0x00020002u, pad0 + 0x00040004u, pad0 + 0x00060006u);
 }
 
 template <int kKpt>
-__device__ __forceinline__ void load_round(int4 (&v)[kKpt / 4], const int4* vec, int64_t ntiles,
-                                           int64_t t0, int64_t nwarps) {
+__device__ __forceinline__ void load_round(int4 (&v)[kKpt / 4], const int4* vec, uint32_t ntiles,
+                                           uint32_t t0, uint32_t nwarps) {
 #pragma unroll
   for (int u = 0; u < kKpt / 4; ++u) {
-    const int64_t t = t0 + u * nwarps;
-    v[u] = t < ntiles ? ld_stream_v4(vec + (t << 5)) : make_int4(-1, -1, -1, -1);
+    const uint32_t t = t0 + u * nwarps;
+    v[u] = t < ntiles ? ld_stream_v4(vec + static_cast<size_t>(t) * 32u) : make_int4(-1, -1, -1, -1);
   }
 }
 
 template <int kKpt, bool kPow2>
-__global__ void __launch_bounds__(1024, 1) cluster_ship_kernel(const ClusterHistArgs a) {
+__global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const ClusterHistArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   Ctx c;
   c.P = cluster_nctarank();
@@ -161,45 +183,68 @@ __global__ void __launch_bounds__(1024, 1) cluster_ship_kernel(const ClusterHist
   c.lgS = 31u - __clz(a.S);
   c.magic = a.magic;
   const uint32_t P = c.P;
-  const uint32_t qs = 8u * a.sub_vectors;   // entries per sub-bucket
-  const uint32_t sb = 2u * qs + 4u;         // bytes per sub-bucket (4-byte skew)
-  const uint32_t cap_vecs = 4u * qs;        // inbox vectors per sender slot
-  c.owner_bytes = 32u * sb;
+  c.PS = P * a.S;
+  const uint32_t qs = 8u * a.sub_vectors;  // rows of an owner block
+  c.blk = 64u * qs;
   const uint32_t cid = cluster_id_x();
 
   // Layout (must match ship_staging_bytes): slice u32[S + 32], cursors
-  // u32[P*32], headers u32[2][16], sub-buckets [P][32] of sb bytes (16-byte
-  // padded in total), inboxes uint4[2][P][4*qs].
+  // u32[2][P + 1][32], headers u32[2][16], sink u16[32], two inbox
+  // mbarriers (256 bytes with padding), staging u16[P][qs][32], inboxes
+  // u16[2][P][qs][32].
   const uint32_t sbase = smem_u32(smem);
   c.slice = sbase;
-  const uint32_t cursor0 = sbase + 4u * (a.S + 32u);
-  const uint32_t header0 = cursor0 + 4u * 32u * P;
-  const uint32_t rows0 = header0 + 4u * 32u;
-  const uint32_t inbox0 = rows0 + ((P * c.owner_bytes + 15u) & ~15u);
-  c.cursor_lane = cursor0 + 4u * c.lane;
-  c.limit_lane = rows0 + c.lane * sb + 2u * qs;
-  uint32_t* cursor = reinterpret_cast<uint32_t*>(smem + (cursor0 - sbase));
-  const uint32_t* header = reinterpret_cast<const uint32_t*>(smem + (header0 - sbase));
+  const uint32_t cur0 = sbase + 4u * (a.S + 32u);
+  const uint32_t header0 = cur0 + 256u * (P + 1u);
+  c.sink = header0 + 128u + 2u * c.lane;
+  const uint32_t full0 = header0 + 192u;  // mbarriers full[2]: inbox buffer complete
+  const uint32_t stage0 = header0 + 256u;
+  const uint32_t inbox0 = stage0 + P * c.blk;
+  c.lim0 = stage0 + c.blk;
+  uint32_t* cursor = reinterpret_cast<uint32_t*>(smem + (cur0 - sbase));
 
-  // Key stream: warp tiles of 32 vectors, kKpt/4 tiles per warp per round.
-  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * 32;
-  const int64_t gwarp = static_cast<int64_t>(blockIdx.x) * 32 + warp;
-  const int64_t ntiles = ((a.n - a.head) >> 2) >> 5;
+  // Key stream: warp tiles of 32 vectors (tile t = vectors 32t .. 32t+31),
+  // kKpt/4 tiles per warp per round; tile indices fit 32 bits (n < 2^39).
+  constexpr uint32_t kWarps = kShipThreads / 32;
+  const uint32_t nwarps = gridDim.x * kWarps;
+  const uint32_t gwarp = blockIdx.x * kWarps + warp;
+  const uint32_t ntiles = static_cast<uint32_t>(((a.n - a.head) >> 2) >> 5);
   const int4* vec = reinterpret_cast<const int4*>(a.keys + a.head) + c.lane;
   constexpr int kTiles = kKpt / 4;
-  const int64_t per_round = nwarps * kTiles;
-  const uint32_t rounds = static_cast<uint32_t>((ntiles + per_round - 1) / per_round);
+  const uint32_t per_round = nwarps * kTiles;
+  const uint32_t rounds = static_cast<uint32_t>((static_cast<uint64_t>(ntiles) + per_round - 1) / per_round);
 
-  // Roles: ns shipper warps per owner, the rest receive.
-  const uint32_t ns = P >= 16 ? 1u : 16u / P;
-  const bool shipper = warp < ns * P;
-  const uint32_t so = shipper ? warp / ns : 0u;      // owner shipped by this warp
-  const uint32_t sh = shipper ? warp % ns : 0u;      // vector phase
-  const uint32_t nrecv = 32u - ns * P;
-  const uint32_t rw = shipper ? 0u : warp - ns * P;
-  const uint32_t dslot = rw % P;                     // sender slot applied by this warp
-  const uint32_t dq = rw / P;
-  const uint32_t dnw = shipper ? 1u : (nrecv - 1u - dslot) / P + 1u;
+  // Ship and apply: warp w serves owner (and sender) w mod P, as member sg of
+  // the sng warps that do; lane l of member sg starts at vector 32*sg + l of
+  // a block and steps by 32*sng vectors.  Every address below is for buffer
+  // (or cursor set) 0; buffer 1 adds a fixed offset.
+  const uint32_t so = warp % P;
+  const uint32_t sg = warp / P;
+  const uint32_t sng = (kWarps - 1u - so) / P + 1u;
+  const uint32_t step = 512u * sng;                          // bytes between a lane's vectors
+  const uint32_t vofs = 16u * (32u * sg + c.lane);           // this lane's first vector
+  const uint32_t set_words = 32u * (P + 1u);
+  const uint32_t set_bytes = 4u * set_words;
+  const uint32_t buf_bytes = P * c.blk;                      // one inbox buffer
+  const uint32_t top = stage0 + so * c.blk;                  // owner so's staging block
+  const uint32_t fill_rd = cur0 + 4u * (32u * so + c.lane);  // cursor (so, lane)
+  const uint32_t col_top = top + 2u * c.lane;                // its initial value
+  const uint32_t hdr_out = map_rank(header0 + 4u * rank, so);
+  const uint32_t dst0 = map_rank(inbox0 + rank * c.blk, so) + vofs;
+  const uint32_t src0 = inbox0 + so * c.blk + vofs;
+  const uint32_t hdr_in = header0 + 4u * so;
+  const uint32_t full_out = map_rank(full0, so);
+  // Cursor reset: thread i < set_words owns word i of a set.
+  const uint32_t rs_row = threadIdx.x >> 5;
+  const uint32_t rs_val = rs_row < P ? stage0 + rs_row * c.blk + 2u * c.lane : kAlwaysFull;
+  const uint32_t rs_addr = cur0 + 4u * threadIdx.x;
+  const bool resets = threadIdx.x < set_words;
+
+  // Padding of this lane: it only ever touches vectors v with v mod 4 ==
+  // lane mod 4, i.e. columns 8*(lane mod 4) .. +7.
+  const uint32_t d0 = a.S + 8u * (c.lane & 3u);
+  const uint32_t pad0 = d0 | ((d0 + 1u) << 16);
+  const uint4 pad = pad_vector(pad0);
 
   for (uint32_t pass = 0; pass < a.passes; ++pass) {
     c.base = pass * P * c.S;
@@ -208,79 +253,85 @@ __global__ void __launch_bounds__(1024, 1) cluster_ship_kernel(const ClusterHist
 
     uint4* s4 = reinterpret_cast<uint4*>(smem);
     for (uint32_t i = threadIdx.x; i < (c.S + 32u) / 4; i += blockDim.x) s4[i] = make_uint4(0, 0, 0, 0);
-    for (uint32_t i = threadIdx.x; i < 32u * P; i += blockDim.x) cursor[i] = rows0 + i * sb;
-    cluster_barrier();  // every slice zeroed before any increment
+    for (uint32_t v = threadIdx.x; v < 4u * qs * P; v += blockDim.x) st_shared_v4(stage0 + 16u * v, pad);
+    for (uint32_t i = threadIdx.x; i < 2u * set_words; i += blockDim.x) {
+      const uint32_t o = (i % set_words) >> 5;
+      cursor[i] = o < P ? stage0 + o * c.blk + 2u * (i & 31u) : kAlwaysFull;
+    }
+    if (threadIdx.x < 32u) st_shared_u32(header0 + 4u * threadIdx.x, 0u);
+    if (threadIdx.x == 0) {
+      // One arrival per sender and round; the senders' bytes complete it.
+      mbar_init(full0, P);
+      mbar_init(full0 + 8u, P);
+      fence_mbar_init();
+    }
+    cluster_barrier();  // slices zeroed and mbarriers initialised cluster-wide
 
     int4 cur[kTiles];
     if (rounds > 0) {
       load_round<kKpt>(cur, vec, ntiles, gwarp, nwarps);
+      c.cur_lane = cur0 + 4u * c.lane;
 #pragma unroll
-      for (int u = 0; u < kTiles; ++u) partition_vec<kPow2>(cur[u], c);
+      for (int u = 0; u < kTiles; ++u) partition_tile<kPow2>(cur[u], c);
     }
     for (uint32_t r = 0; r < rounds; ++r) {
       const bool more = r + 1 < rounds;
-      if (more) load_round<kKpt>(cur, vec, ntiles, gwarp + static_cast<int64_t>(r + 1) * per_round, nwarps);
-      __syncthreads();  // partition of round r complete
+      if (more) load_round<kKpt>(cur, vec, ntiles, gwarp + (r + 1) * per_round, nwarps);
       const uint32_t buf = r & 1u;
-      if (shipper) {
-        // B: close owner so's sub-bucket `lane`, ship vectors j = sh (mod ns).
-        const uint32_t sub = so * 32u + c.lane;
-        const uint32_t col = rows0 + sub * sb;
-        const uint32_t fill = (cursor[sub] - col) >> 1;
-        const uint32_t cnt = fill < qs ? fill : qs;
-        const uint32_t nv = (cnt + 7u) >> 3;
-        if (sh == 0)  // pad the last vector with this lane's dummy counter
-          for (uint32_t p = cnt; p < 8u * nv; ++p)
-            st_shared_u16(col + 2u * p, static_cast<uint16_t>(c.S + c.lane));
-        if (ns > 1) named_barrier(1, 32u * ns * P);  // cursors read, padding written
-        if (sh == 0) cursor[sub] = col;
-        uint32_t incl = nv;
-#pragma unroll
-        for (uint32_t d = 1; d < 32; d <<= 1) {
-          const uint32_t t = __shfl_up_sync(0xffffffffu, incl, d);
-          if (c.lane >= d) incl += t;
+      // The cluster barrier's arrivals precede the partition, so only this
+      // barrier orders the partition before the ship.
+      __syncthreads();  // round r staged
+      {
+        // Ship owner so's block of this round: rows = its fullest column.
+        const uint32_t fill = (ld_shared_u32(fill_rd + buf * set_bytes) - col_top) >> 6;
+        const uint32_t rows = __reduce_max_sync(kFullMask, min(fill, qs));
+        const uint32_t mbar = full_out + 8u * buf;
+        if (sg == 0 && c.lane == 0) {
+          mbar_arrive_expect_tx_remote(mbar, 64u * rows + 4u);
+          st_async_u32(hdr_out + 64u * buf, rows, mbar);
         }
-        const uint32_t dst = inbox0 + 16u * ((buf * P + rank) * cap_vecs + incl - nv);
-        for (uint32_t j = sh; j < nv; j += ns) {
-          const uint32_t a4 = col + 16u * j;  // 4-byte aligned
-          uint4 x;
-          asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x.x) : "r"(a4));
-          asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x.y) : "r"(a4 + 4u));
-          asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x.z) : "r"(a4 + 8u));
-          asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x.w) : "r"(a4 + 12u));
-          st_cluster_v4(map_rank(dst + 16u * j, so), x);
+        const uint32_t end = top + 64u * rows;
+        for (uint32_t at = top + vofs, dt = dst0 + buf * buf_bytes; at < end; at += step, dt += step) {
+          st_async_v4(dt, ld_shared_v4(at), mbar);
+          st_shared_v4(at, pad);
         }
-        if (sh == 0 && c.lane == 31)
-          st_cluster_u32(map_rank(header0 + 4u * (buf * 16u + rank), so), incl);
-      } else if (r > 0) {
-        // D: apply the previous round's inbox from sender slot `dslot`.
+      }
+      if (r > 0) {
+        // Apply sender so's block of the previous round, once every sender
+        // has arrived and every byte has landed.
         const uint32_t pb = buf ^ 1u;
-        const uint32_t nvec = header[pb * 16u + dslot];
-        const uint32_t src0 = inbox0 + 16u * ((pb * P + dslot) * cap_vecs);
-        for (uint32_t v = dq * 32u + c.lane; v < nvec; v += dnw * 32u)
-          apply_vector(c.slice, ld_shared_v4(src0 + 16u * v));
+        if (wait_inbox(full0 + 8u * pb, ((r - 1u) >> 1) & 1u)) {
+          const uint32_t src = src0 + pb * buf_bytes;
+          const uint32_t end = src - vofs + 64u * min(ld_shared_u32(hdr_in + 64u * pb), qs);
+          for (uint32_t at = src; at < end; at += step) apply_vector(c.slice, ld_shared_v4(at));
+        }
       }
-      __syncthreads();  // rows read and cursors reset before the next partition
-      if (!shipper) cluster_arrive_relaxed();
+      __syncthreads();  // staging shipped and re-padded; this round's cursors read
+      if (resets) st_shared_u32(rs_addr + buf * set_bytes, rs_val);
+      // Relaxed: inbox data is published through the mbarriers; this
+      // barrier only tells senders that round r-1's inbox has been read
+      // (every load of it has returned: its values fed the reds above).
+      cluster_arrive_relaxed();
       if (more) {
+        c.cur_lane = cur0 + 4u * c.lane + (buf ^ 1u) * set_bytes;
 #pragma unroll
-        for (int u = 0; u < kTiles; ++u) partition_vec<kPow2>(cur[u], c);
+        for (int u = 0; u < kTiles; ++u) partition_tile<kPow2>(cur[u], c);
       }
-      if (shipper) cluster_arrive();
-      cluster_wait();  // round r's inboxes complete everywhere
+      cluster_wait();  // round r's inboxes complete everywhere; round r+1 staged
     }
-    if (rounds > 0 && !shipper) {
+    if (rounds > 0) {
       const uint32_t pb = (rounds - 1u) & 1u;
-      const uint32_t nvec = header[pb * 16u + dslot];
-      const uint32_t src0 = inbox0 + 16u * ((pb * P + dslot) * cap_vecs);
-      for (uint32_t v = dq * 32u + c.lane; v < nvec; v += dnw * 32u)
-        apply_vector(c.slice, ld_shared_v4(src0 + 16u * v));
+      if (wait_inbox(full0 + 8u * pb, ((rounds - 1u) >> 1) & 1u)) {
+        const uint32_t src = src0 + pb * buf_bytes;
+        const uint32_t end = src - vofs + 64u * min(ld_shared_u32(hdr_in + 64u * pb), qs);
+        for (uint32_t at = src; at < end; at += step) apply_vector(c.slice, ld_shared_v4(at));
+      }
     }
 
     // Ragged keys (unaligned head, partial tile, tail): the grid's last warp,
     // straight to the owners.
     if (gwarp == nwarps - 1) {
-      const int64_t after = a.head + (ntiles << 7);
+      const int64_t after = a.head + (static_cast<int64_t>(ntiles) << 7);
       const int64_t leftover = static_cast<int64_t>(a.head) + (a.n - after);
       for (int64_t j = c.lane; j < leftover; j += 32) {
         const int32_t key = a.keys[j < a.head ? j : after + (j - a.head)];
@@ -294,6 +345,10 @@ __global__ void __launch_bounds__(1024, 1) cluster_ship_kernel(const ClusterHist
     }
 
     cluster_barrier();  // every increment has landed; only own memory after this
+    if (threadIdx.x == 0) {
+      mbar_inval(full0);
+      mbar_inval(full0 + 8u);
+    }
 
     const uint32_t first = c.base + rank * c.S;
     if (c.range > rank * c.S) {
@@ -330,6 +385,13 @@ bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
 }  // namespace
 
+cudaError_t read_and_clear_ship_status(uint32_t* out) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_ship_status, sizeof(uint32_t));
+  if (e != cudaSuccess) return e;
+  const uint32_t zero = 0;
+  return *out ? cudaMemcpyToSymbol(g_ship_status, &zero, sizeof(uint32_t)) : cudaSuccess;
+}
+
 cudaError_t prepare_ship_kernel(int kpt, int smem_bytes) {
   for (int p2 = 0; p2 < 2; ++p2) {
     const void* fn = ship_kernel_ptr(kpt, p2 != 0);
@@ -344,7 +406,7 @@ cudaError_t prepare_ship_kernel(int kpt, int smem_bytes) {
 cudaError_t query_ship_active_clusters(int kpt, int cluster_size, int smem_bytes, int* out) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cluster_size, 1, 1);
-  cfg.blockDim = dim3(1024, 1, 1);
+  cfg.blockDim = dim3(kShipThreads, 1, 1);
   cfg.dynamicSmemBytes = smem_bytes;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -360,7 +422,7 @@ cudaError_t launch_cluster_ship(const dsmem_hist_plan_t& plan, const ClusterHist
                                 cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(plan.num_clusters) * plan.cluster_size, 1, 1);
-  cfg.blockDim = dim3(1024, 1, 1);
+  cfg.blockDim = dim3(kShipThreads, 1, 1);
   cfg.dynamicSmemBytes = plan.smem_bytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

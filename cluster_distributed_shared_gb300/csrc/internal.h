@@ -7,6 +7,7 @@
 
 #include "dsmem_hist.h"
 
+
 namespace dsmh {
 
 // Keys every thread handles per unrolled step of the streaming loop: four
@@ -21,6 +22,8 @@ constexpr int kMinStepsPerCta = 4;
 constexpr int kDefaultSliceCapBytes = 128 * 1024;
 // Scratch bound the planner keeps the partial rows under when it picks C.
 constexpr int64_t kMaxAutoScratchBytes = int64_t{1} << 30;
+// Threads per CTA of the ship kernel.
+constexpr int kShipThreads = DSMEM_HIST_SHIP_THREADS;
 // Shared memory the runtime reserves per CTA on sm_90 and later.
 constexpr int kSmemReservedPerCta = 1024;
 
@@ -58,6 +61,9 @@ cudaError_t query_ship_active_clusters(int keys_per_thread, int cluster_size, in
                                        int* out);
 cudaError_t launch_cluster_ship(const dsmem_hist_plan_t& plan, const ClusterHistArgs& args,
                                 cudaStream_t stream);
+// Reads (synchronously) and clears the ship kernel's device status word on
+// the current device: bit 0 = a bounded inbox wait gave up.
+cudaError_t read_and_clear_ship_status(uint32_t* out);
 
 // Sets the kernel attributes a shape needs (dynamic shared memory above
 // 48 KiB, non-portable cluster sizes) on the current device.

@@ -32,16 +32,14 @@ namespace dsmh {
 uint64_t owner_magic(uint32_t S) { return ((uint64_t{1} << 40) / S) + 1; }
 
 // Shared memory the ship kernel needs beside the slice; the kernel lays it
-// out in this order: 32 dummy counters after the slice (targets of padding
-// entries), cursors u32[P*32], inbox headers u32[2][16], sub-buckets [P][32]
-// of 2*qs + 4 bytes (qs = 8*sub_vectors entries; total rounded up to 16
-// bytes), inboxes uint4[2][P][32*sub_vectors].
+// out in this order: 32 padding counters after the slice, two cursor sets
+// u32[P + 1][32], inbox headers u32[2][16] plus a 16-bit sink per lane (256
+// bytes in all), the staging blocks u16[P][qs][32] and the inboxes
+// u16[2][P][qs][32] (qs = 8 * sub_vectors rows of 64 bytes).
 uint32_t ship_staging_bytes(int cluster_size, int sub_vectors) {
   const uint32_t P = static_cast<uint32_t>(cluster_size), nq = static_cast<uint32_t>(sub_vectors);
-  const uint32_t buckets = (P * 32u * (16u * nq + 4u) + 15u) & ~15u;
-  return 4u * 32u + 4u * 32u * P + 4u * 32u + buckets + 16u * 2u * P * 32u * nq;
+  return 4u * 32u + 8u * 32u * (P + 1u) + 256u + 3u * P * 64u * 8u * nq;
 }
-
 
 static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -112,11 +110,11 @@ int plan_shape(const dsmem_hist_device_t* dev, int32_t num_bins, int64_t n,
   // Kernel choice: shipping whenever the cluster has remote owners and its
   // staging fits beside the slice (1024 threads), else direct increments.
   int kernel = DSMEM_HIST_KERNEL_DIRECT, kpt = 0, nq = 0;
-  const bool ship_ok_threads = req->block_threads == 0 || req->block_threads == 1024;
+  const bool ship_ok_threads = req->block_threads == 0 || req->block_threads == kShipThreads;
   if (req->kernel == DSMEM_HIST_KERNEL_SHIP || (req->kernel < 0 && P >= 2 && ship_ok_threads)) {
     if (P < 2 || !ship_ok_threads) {
       if (req->kernel == DSMEM_HIST_KERNEL_SHIP) {
-        *why = "the ship kernel needs cluster_size >= 2 and 1024 threads";
+        *why = "the ship kernel needs cluster_size >= 2 and its fixed block size";
         return DSMEM_HIST_EINVAL;
       }
     } else {
@@ -125,7 +123,7 @@ int plan_shape(const dsmem_hist_device_t* dev, int32_t num_bins, int64_t n,
       // round before 4.
       for (int t = 0; t < 4 && !kernel; ++t) {
         const int k = t < 2 ? 8 : 4;
-        const int64_t expect = 32 * k;  // entries per sub-bucket per round, times P
+        const int64_t expect = (kShipThreads / 32) * k;  // entries per column per round, times P
         const int q = static_cast<int>(ceil_div((t % 2 == 0 ? 2 * expect : 3 * expect / 2), 8 * P));
         const int64_t need = 4 * S + ship_staging_bytes(P, q);
         if (need <= dev->max_smem_per_block_optin &&
@@ -145,7 +143,7 @@ int plan_shape(const dsmem_hist_device_t* dev, int32_t num_bins, int64_t n,
 
   int threads;
   if (kernel == DSMEM_HIST_KERNEL_SHIP) {
-    threads = 1024;
+    threads = kShipThreads;
   } else if (req->block_threads != 0) {
     threads = req->block_threads;
   } else {

@@ -57,6 +57,52 @@ __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// mbarrier helpers (shared::cta addresses unless noted).
+__device__ __forceinline__ void mbar_init(uint32_t addr, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(addr), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_inval(uint32_t addr) {
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(addr) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// Arrives on an mbarrier of a CTA of the cluster (shared::cluster address)
+// and adds `bytes` to its pending transaction count.
+__device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t cluster_addr, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
+                   cluster_addr),
+               "r"(bytes)
+               : "memory");
+}
+// One probe of phase `parity`; true once that phase has completed.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Asynchronous stores into a peer CTA's shared memory; their completion is
+// counted (in bytes) on the peer's mbarrier `cluster_mbar`, not by this thread.
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, const uint4& v,
+                                            uint32_t cluster_mbar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+          cluster_addr),
+      "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(cluster_mbar)
+      : "memory");
+}
+__device__ __forceinline__ void st_async_u32(uint32_t cluster_addr, uint32_t v, uint32_t cluster_mbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(cluster_addr),
+               "r"(v), "r"(cluster_mbar)
+               : "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -100,6 +146,18 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t cta_addr) {
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "r"(cta_addr));
+  return v;
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t cta_addr, const uint4& v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(cta_addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w));
+}
+__device__ __forceinline__ void st_shared_u32(uint32_t cta_addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(cta_addr), "r"(v));
+}
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t cta_addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(cta_addr));
   return v;
 }
 __device__ __forceinline__ void st_shared_u16(uint32_t cta_addr, uint16_t v) {

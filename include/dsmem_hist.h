@@ -60,8 +60,11 @@ enum {
  *           with __match_any_sync warp aggregation).
  *   SHIP:   keys travel to their owner as 16-bit local indices in coalesced
  *           16-byte DSMEM stores and the owner applies local shared-memory
- *           atomics (1024 threads per CTA; P >= 2). */
+ *           atomics (DSMEM_HIST_SHIP_THREADS threads per CTA; P >= 2). */
 enum { DSMEM_HIST_KERNEL_DIRECT = 0, DSMEM_HIST_KERNEL_SHIP = 1 };
+
+/* Threads per CTA of the ship kernel (fixed at build time). */
+#define DSMEM_HIST_SHIP_THREADS 768
 
 /* Launch shape chosen by the planner (all fields filled by dsmem_hist_plan*). */
 typedef struct dsmem_hist_plan {
@@ -77,7 +80,8 @@ typedef struct dsmem_hist_plan {
   int32_t max_active_clusters; /* occupancy answer for this shape (0 when not queried) */
   int32_t kernel;              /* DSMEM_HIST_KERNEL_DIRECT or DSMEM_HIST_KERNEL_SHIP */
   int32_t keys_per_thread;     /* ship kernel: keys each thread partitions per round (4 or 8) */
-  int32_t sub_vectors;         /* ship kernel: 16-byte vectors per (owner, lane) sub-bucket */
+  int32_t sub_vectors;         /* ship kernel: rows of each owner's staging block, in units
+                                  of 8 (each row: 32 columns of 16-bit entries) */
   int32_t reserved;            /* zero */
   int64_t partial_stride;      /* u32 elements between two clusters' partial rows (num_bins rounded up to 4) */
   int64_t workspace_bytes;     /* scratch: num_clusters * partial_stride * 4 */
@@ -252,6 +256,17 @@ DSMEM_HIST_API const char* dsmem_hist_last_error(void);
  * events) on every device it touched.  Call only when no dsmem_hist work is
  * in flight; later calls recreate what they need. */
 DSMEM_HIST_API void dsmem_hist_release(void);
+
+/* Reads and clears the current device's status word of the key-shipping
+ * kernel (DSMEM_HIST_KERNEL_SHIP).  That kernel waits for its peers' inbox
+ * bytes with bounded waits (about 50 ms each); a wait that gives up sets bit 0
+ * of the word and skips that inbox, so the histogram of that launch is wrong.
+ * *status (may be NULL) receives the word.  Synchronous: it reads the word
+ * with cudaMemcpyFromSymbol on the legacy default stream.  Returns
+ * DSMEM_HIST_OK if the word was 0, DSMEM_HIST_ETIMEOUT if a wait gave up since
+ * the last call, DSMEM_HIST_ECUDA on a CUDA error.  No counterpart in the
+ * pages' design, which waits only on cluster barriers. */
+DSMEM_HIST_API int dsmem_hist_device_status(uint32_t* status);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 DSMEM_HIST_API int dsmem_hist_version(void);

@@ -82,7 +82,7 @@ def plan(dev, nb, n, mac=0, **kw):
 def test_planner_matches_published_cluster_shapes(nb, n, P, S):
     p = plan(GB300, nb, n, cluster_size=P)
     assert (p["cluster_size"], p["bins_per_cta"], p["passes"]) == (P, S, 1)
-    assert p["kernel"] == pkg.KERNEL_SHIP and p["block_threads"] == 1024
+    assert p["kernel"] == pkg.KERNEL_SHIP and p["block_threads"] == pkg.SHIP_THREADS
     assert 4 * S < p["smem_bytes"] <= GB300["max_smem_per_block_optin"]
     q = plan(GB300, nb, n)          # the planner's own choice agrees here
     assert (q["cluster_size"], q["bins_per_cta"]) == (P, S)
@@ -107,9 +107,10 @@ def test_planner_covers_every_bin(nb, slice_cap):
         assert p["workspace_bytes"] == p["num_clusters"] * p["partial_stride"] * 4
         assert p["smem_bytes"] <= GB300["max_smem_per_block_optin"]
         if p["kernel"] == pkg.KERNEL_SHIP:
-            assert P >= 2 and p["block_threads"] == 1024 and p["keys_per_thread"] in (4, 8)
+            assert P >= 2 and p["block_threads"] == pkg.SHIP_THREADS
+            assert p["keys_per_thread"] in (4, 8)
             nq = p["sub_vectors"]
-            assert nq >= 1 and 8 * nq * 32 * P >= 1.5 * 1024 * p["keys_per_thread"]
+            assert nq >= 1 and 8 * nq * 32 * P >= 1.5 * pkg.SHIP_THREADS * p["keys_per_thread"]
             assert p["smem_bytes"] == 4 * S + ship_staging(P, nq)
             assert S < 0xFFFF                               # 16-bit local indices + sentinel
         else:
@@ -119,9 +120,10 @@ def test_planner_covers_every_bin(nb, slice_cap):
 
 
 def ship_staging(P, nq):
-    # dummy counters, cursors, headers, skewed sub-buckets, double inbox
-    buckets = (P * 32 * (16 * nq + 4) + 15) // 16 * 16
-    return 4 * 32 + 4 * 32 * P + 4 * 32 + buckets + 16 * 2 * P * 32 * nq
+    # padding counters, two cursor sets of P + 1 rows, headers + sink,
+    # staging blocks and two inboxes of 8 * nq rows of 64 bytes per owner
+    rows = 8 * nq
+    return 4 * 32 + 2 * 4 * 32 * (P + 1) + 256 + 3 * P * rows * 64
 
 
 @pytest.mark.parametrize("P", range(2, 17))
@@ -130,8 +132,8 @@ def test_ship_plan_fits_for_every_cluster_size(P):
         p = plan(GB300, nb, 1 << 26, cluster_size=P, kernel=pkg.KERNEL_SHIP)
         assert p["kernel"] == pkg.KERNEL_SHIP
         assert p["smem_bytes"] + 1024 <= GB300["max_smem_per_sm"]
-        # sub-buckets hold at least 1.5 times the expected keys per (owner, lane) and round
-        expected = 32 * p["keys_per_thread"] / P
+        # staging columns hold at least 1.5 times the expected keys per (owner, lane) and round
+        expected = pkg.SHIP_THREADS // 32 * p["keys_per_thread"] / P
         assert 8 * p["sub_vectors"] >= 1.5 * expected
 
 
@@ -143,15 +145,16 @@ def test_owner_magic_exact():
         magic = (1 << 40) // S + 1
         P = 16
         rels = list(range(0, min(P * S, 200000))) + list(range(max(0, P * S - 200000), P * S))
-        for rel in rels[:: max(1, len(rels) // 50000)] + [P * S - 1]:
-            assert (rel * magic) >> 40 == rel // S, (S, rel)
+        for rel in rels[:: max(1, len(rels) // 50000)] + [P * S - 1, P * S]:
+            assert (rel * magic) >> 40 == rel // S, (S, rel)   # P * S: the clamp value
 
 
 def test_planner_grid_and_threads():
     p = plan(GB300, 262144, 1 << 28, mac=16)
-    assert p["num_clusters"] == 16 and p["block_threads"] == 1024 and p["ctas_per_sm"] == 1
+    assert p["num_clusters"] == 16 and p["block_threads"] == pkg.SHIP_THREADS
+    assert p["ctas_per_sm"] == 1
     small = plan(GB300, 8192, 1000, mac=100)
-    assert small["num_clusters"] == 1 and small["block_threads"] == 1024
+    assert small["num_clusters"] == 1 and small["block_threads"] == pkg.SHIP_THREADS
     direct = plan(GB300, 8192, 1000, mac=100, kernel=pkg.KERNEL_DIRECT)
     assert direct["block_threads"] == 512 and direct["kernel"] == pkg.KERNEL_DIRECT
     one = plan(GB300, 8192, 1 << 20, cluster_size=1)
@@ -210,3 +213,10 @@ def test_tune_and_microbench_reject_bad_arguments():
     v, ms = ctypes.c_double(), ctypes.c_double()
     assert L.dsmem_hist_microbench(0, 17, 16, ctypes.byref(v), ctypes.byref(ms)) == pkg.DSMEM_HIST_EINVAL
     assert L.dsmem_hist_microbench(0, 2, 0, ctypes.byref(v), ctypes.byref(ms)) == pkg.DSMEM_HIST_EINVAL
+
+
+def test_ship_threads_match_header():
+    header = open(os.path.join(ROOT, "include", "dsmem_hist.h")).read()
+    m = re.search(r"^#define DSMEM_HIST_SHIP_THREADS (\d+)", header, re.M)
+    assert m and int(m.group(1)) == pkg.SHIP_THREADS
+    assert pkg.SHIP_THREADS % 32 == 0 and 32 * 17 <= pkg.SHIP_THREADS <= 1024
