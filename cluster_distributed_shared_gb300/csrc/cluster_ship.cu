@@ -89,42 +89,67 @@ __device__ __forceinline__ void owner_local(uint32_t rel, const Ctx& c, uint32_t
   }
 }
 
+// Stores a 16-bit entry at `ea` if `ea` is below its block's end `lim`,
+// else counts a spill; predicated, without a branch.
+__device__ __forceinline__ void stage_entry(uint32_t ea, uint32_t lim, uint32_t loc, uint32_t& spill) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.lt.u32 p, %1, %2;\n\t"
+      "@p st.shared.u16 [%1], %3;\n\t"
+      "@!p add.u32 %0, %0, 1;\n\t}"
+      : "+r"(spill)
+      : "r"(ea), "r"(lim), "h"(static_cast<uint16_t>(loc)));
+}
+
 // Partition one warp tile (four keys per lane).  All four reservations are
-// issued before the first store so their latencies overlap.
-template <bool kPow2>
+// issued before the first store so their latencies overlap.  kBase0: the
+// pass starts at bin 0, so a key is its own in-pass offset.
+template <bool kPow2, bool kBase0>
 __device__ __forceinline__ void partition_tile(const int4& v, const Ctx& c) {
   const bool eq4 = (v.x == v.y) & (v.y == v.z) & (v.z == v.w);
-  const int32_t k0 = __shfl_sync(kFullMask, v.x, 0);
-  if (__all_sync(kFullMask, eq4 & (v.x == k0))) {
-    const uint32_t rel = static_cast<uint32_t>(k0) - c.base;
-    if (c.lane == 0 && rel < c.range) {
-      uint32_t o, loc;
-      owner_local(rel, c, o, loc, kPow2);
-      red_add_cluster(map_rank(c.slice + 4u * loc, o), 128u);
+  if (__all_sync(kFullMask, eq4)) {  // rare on most inputs: then test the whole tile
+    const int32_t k0 = __shfl_sync(kFullMask, v.x, 0);
+    if (__all_sync(kFullMask, v.x == k0)) {
+      const uint32_t rel = static_cast<uint32_t>(k0) - (kBase0 ? 0u : c.base);
+      if (c.lane == 0 && rel < c.range) {
+        uint32_t o, loc;
+        owner_local(rel, c, o, loc, kPow2);
+        red_add_cluster(map_rank(c.slice + 4u * loc, o), 128u);
+      }
+      return;
     }
-    return;
   }
   const int32_t keys[4] = {v.x, v.y, v.z, v.w};
   uint32_t own[4], loc[4], ea[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     // Offsets at or past P*S clamp to owner P, the always-full cursor row.
-    const uint32_t rel = min(static_cast<uint32_t>(keys[k]) - c.base, c.PS);
+    const uint32_t rel = min(static_cast<uint32_t>(keys[k]) - (kBase0 ? 0u : c.base), c.PS);
     owner_local(rel, c, own[k], loc[k], kPow2);
     ea[k] = atom_add_local(c.cur_lane + (own[k] << 7), 64u);
   }
   uint32_t spill = 0;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const bool ok = ea[k] < c.lim0 + own[k] * c.blk;
-    st_shared_u16(ok ? ea[k] : c.sink, static_cast<uint16_t>(loc[k]));
-    spill |= ok ? 0u : (1u << k);
-  }
+  for (int k = 0; k < 4; ++k) stage_entry(ea[k], c.lim0 + own[k] * c.blk, loc[k], spill);
   if (__any_sync(kFullMask, spill != 0)) {
+    // Rare: redo the test per key and send each spilled in-range key to its owner.
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-      if (((spill >> k) & 1u) && static_cast<uint32_t>(keys[k]) - c.base < c.range)
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t rel = static_cast<uint32_t>(keys[k]) - (kBase0 ? 0u : c.base);
+      if (ea[k] >= c.lim0 + own[k] * c.blk && rel < c.range)
         red_add_cluster(map_rank(c.slice + 4u * loc[k], own[k]), 1u);
+    }
+  }
+}
+
+template <int kTiles, bool kPow2>
+__device__ __forceinline__ void partition_round(const int4 (&v)[kTiles], const Ctx& c) {
+  if (c.base == 0) {
+#pragma unroll
+    for (int u = 0; u < kTiles; ++u) partition_tile<kPow2, true>(v[u], c);
+  } else {
+#pragma unroll
+    for (int u = 0; u < kTiles; ++u) partition_tile<kPow2, false>(v[u], c);
   }
 }
 
@@ -161,9 +186,16 @@ __device__ __forceinline__ uint4 pad_vector(uint32_t pad0) {
   return make_uint4(pad0, pad0 + 0x00020002u, pad0 + 0x00040004u, pad0 + 0x00060006u);
 }
 
+// Loads a round's tiles t0 + u * nwarps; tiles past the end read as keys -1
+// (outside every pass).  Only the last round can reach past the end.
 template <int kKpt>
 __device__ __forceinline__ void load_round(int4 (&v)[kKpt / 4], const int4* vec, uint32_t ntiles,
-                                           uint32_t t0, uint32_t nwarps) {
+                                           uint32_t t0, uint32_t nwarps, bool last) {
+  if (!last) {
+#pragma unroll
+    for (int u = 0; u < kKpt / 4; ++u) v[u] = ld_stream_v4(vec + static_cast<size_t>(t0 + u * nwarps) * 32u);
+    return;
+  }
 #pragma unroll
   for (int u = 0; u < kKpt / 4; ++u) {
     const uint32_t t = t0 + u * nwarps;
@@ -269,14 +301,13 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
 
     int4 cur[kTiles];
     if (rounds > 0) {
-      load_round<kKpt>(cur, vec, ntiles, gwarp, nwarps);
+      load_round<kKpt>(cur, vec, ntiles, gwarp, nwarps, rounds == 1);
       c.cur_lane = cur0 + 4u * c.lane;
-#pragma unroll
-      for (int u = 0; u < kTiles; ++u) partition_tile<kPow2>(cur[u], c);
+      partition_round<kTiles, kPow2>(cur, c);
     }
     for (uint32_t r = 0; r < rounds; ++r) {
       const bool more = r + 1 < rounds;
-      if (more) load_round<kKpt>(cur, vec, ntiles, gwarp + (r + 1) * per_round, nwarps);
+      if (more) load_round<kKpt>(cur, vec, ntiles, gwarp + (r + 1) * per_round, nwarps, r + 2 == rounds);
       const uint32_t buf = r & 1u;
       // The cluster barrier's arrivals precede the partition, so only this
       // barrier orders the partition before the ship.
@@ -314,8 +345,7 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
       cluster_arrive_relaxed();
       if (more) {
         c.cur_lane = cur0 + 4u * c.lane + (buf ^ 1u) * set_bytes;
-#pragma unroll
-        for (int u = 0; u < kTiles; ++u) partition_tile<kPow2>(cur[u], c);
+        partition_round<kTiles, kPow2>(cur, c);
       }
       cluster_wait();  // round r's inboxes complete everywhere; round r+1 staged
     }
