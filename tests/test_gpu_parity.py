@@ -155,6 +155,26 @@ def test_ship_overflow_and_runs_paths():
             assert np.array_equal(got, want), (num_bins, P, kw)
 
 
+def test_ship_mostly_out_of_range_and_multi_pass():
+    # Keys outside the pass meet the always-full cursor row and leave through
+    # the spill path on almost every tile; later passes subtract their base.
+    rng = np.random.default_rng(11)
+    n = 3_000_017
+    num_bins = 262144
+    keys = rng.integers(-2 ** 31, 2 ** 31 - 1, n, dtype=np.int64).astype(np.int32)
+    keys[::10] = rng.integers(0, num_bins, keys[::10].size)               # 10% in range
+    want = oracle.histogram(keys, num_bins)
+    for P in (3, 8, 16):
+        got = gpu_hist(keys, num_bins, cluster_size=P, kernel=SH)
+        assert np.array_equal(got, want), P
+    for num_bins, P in [(1 << 21, 8), (600_001, 4), (1 << 20, 2)]:
+        keys = gen.uniform(n, num_bins + 1000, seed=num_bins)
+        plan = pkg.dsmem_hist_plan(num_bins, n, cluster_size=P, kernel=SH)
+        assert plan["kernel"] == SH and plan["passes"] > 1, plan
+        got = gpu_hist(keys, num_bins, cluster_size=P, kernel=SH)
+        assert np.array_equal(got, oracle.histogram(keys, num_bins)), (num_bins, P)
+
+
 def test_multi_pass_bin_ranges():
     n = 3_000_001
     for num_bins, kw in [(1 << 22, {}), (100003, dict(max_slice_bytes=4096)),
