@@ -328,17 +328,21 @@ MICROBENCH_KINDS = {
     "remote_st16_scattered": 2,
     "remote_st16_coalesced": 3,
     "cluster_barrier": 4,
+    "dsmem_pingpong": 5,
+    "gmem_pingpong": 6,
 }
 
 
 def dsmem_hist_microbench(kind: str, cluster_size: int, iters: int = 4096) -> dict:
-    """One DSMEM primitive's rate on the current GPU (see the C header):
-    ops (or bytes) per clock per SM, or cycles per cluster barrier."""
+    """One DSMEM primitive on the current GPU (see the C header): ops (or
+    bytes) per clock per SM, cycles per cluster barrier, or cycles per
+    one-way ping-pong hop."""
     value, ms = ctypes.c_double(0), ctypes.c_double(0)
     _check(lib().dsmem_hist_microbench(MICROBENCH_KINDS[kind], int(cluster_size), int(iters),
                                        ctypes.byref(value), ctypes.byref(ms)))
     unit = {"cluster_barrier": "cycles/barrier", "remote_st16_scattered": "bytes/clk/SM",
-            "remote_st16_coalesced": "bytes/clk/SM"}.get(kind, "ops/clk/SM")
+            "remote_st16_coalesced": "bytes/clk/SM", "dsmem_pingpong": "cycles/hop",
+            "gmem_pingpong": "cycles/hop"}.get(kind, "ops/clk/SM")
     return {"kind": kind, "cluster_size": cluster_size, "value": value.value, "unit": unit,
             "ms": ms.value}
 

@@ -4,11 +4,12 @@
 // ping-pong sections) and "CREDIT" (microbenchmark section: remote versus
 // local access) measured on Hopper.
 //
-// Every kernel runs 1024 threads per CTA with 128 KiB of dynamic shared
+// Every rate kernel runs 1024 threads per CTA with 128 KiB of dynamic shared
 // memory (one CTA per SM), as many clusters as can be resident, and times
 // its loop with clock64 per CTA.  Addresses stay inside the 32768-counter
 // slice; every thread reaches the closing cluster barrier, so no CTA exits
-// while a peer may still touch its shared memory.
+// while a peer may still touch its shared memory.  The ping-pong kernels run
+// one cluster and time one thread's round trips.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -58,6 +59,104 @@ __global__ void __launch_bounds__(1024, 1) probe_kernel(int iters, unsigned long
   cluster_barrier();
   if (threadIdx.x == 0) cycles[blockIdx.x] = static_cast<unsigned long long>(t1 - t0);
   if (slice[threadIdx.x & (kSlice - 1u)] == 0xFFFFFFFFu) sink[0] = x;
+}
+
+// Ping-pong between thread 0 of CTA 0 and thread 0 of CTA 1 of one
+// cluster: round k, CTA 0 stores k into CTA 1's flag and waits for CTA 1 to
+// store k into its own.  Flags live in the receiver's shared memory
+// (kGlobal = false) or in `gflags` (kGlobal = true).  Every poll loop is
+// bounded; a loop that gives up sets sink[1] and ends the test on both sides
+// (the peer then gives up too, after at most its own bound).
+template <bool kGlobal>
+__global__ void pingpong_kernel(int iters, unsigned long long* cycles, uint32_t* sink,
+                                uint32_t* gflags) {
+  __shared__ uint32_t flag;
+  const uint32_t rank = cluster_ctarank();
+  if (threadIdx.x == 0) flag = 0;
+  cluster_barrier();
+  constexpr uint32_t kPolls = 1u << 20;
+  if (threadIdx.x == 0 && rank < 2) {
+    const uint32_t peer = rank ^ 1u;
+    const uint32_t mine = smem_u32(&flag);
+    const uint32_t theirs = map_rank(mine, peer);
+    uint32_t* gmine = gflags + rank;
+    uint32_t* gtheirs = gflags + peer;
+    bool ok = true;
+    const long long t0 = clock64();
+    for (uint32_t k = 1; ok && k <= static_cast<uint32_t>(iters); ++k) {
+      if (rank == 0) {
+        if (kGlobal) st_release_gpu(gtheirs, k);
+        else st_release_cluster(theirs, k);
+      }
+      uint32_t polls = 0, seen = 0;
+      do {
+        seen = kGlobal ? ld_acquire_gpu(gmine) : ld_acquire_cluster(mine);
+      } while (seen < k && ++polls < kPolls);
+      if (seen < k) {
+        ok = false;
+        atomicOr(sink + 1, 1u);
+        break;
+      }
+      if (rank == 1) {
+        if (kGlobal) st_release_gpu(gtheirs, k);
+        else st_release_cluster(theirs, k);
+      }
+    }
+    const long long t1 = clock64();
+    if (rank == 0) cycles[0] = static_cast<unsigned long long>(t1 - t0);
+  }
+  cluster_barrier();  // no CTA exits while its peer may still store into it
+}
+
+template <bool kGlobal>
+cudaError_t run_pingpong(int cluster_size, int iters, double* hop_cycles, double* ms, bool* timed_out) {
+  auto fn = pingpong_kernel<kGlobal>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster_size;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.blockDim = dim3(32);
+  cfg.gridDim = dim3(cluster_size);
+  unsigned long long* cycles = nullptr;
+  uint32_t* buf = nullptr;  // sink[2], then the two global flags
+  if ((e = cudaMalloc(&cycles, sizeof(unsigned long long))) != cudaSuccess) return e;
+  if ((e = cudaMalloc(&buf, 4 * sizeof(uint32_t))) != cudaSuccess) {
+    cudaFree(cycles);
+    return e;
+  }
+  cudaEvent_t a = nullptr, b = nullptr;
+  cudaEventCreate(&a);
+  cudaEventCreate(&b);
+  uint32_t host[2] = {0, 0};
+  for (int run = 0; run < 2 && e == cudaSuccess; ++run) {  // warm-up, then the timed run
+    if ((e = cudaMemset(buf, 0, 4 * sizeof(uint32_t))) != cudaSuccess) break;
+    cudaEventRecord(a);
+    e = cudaLaunchKernelEx(&cfg, fn, iters, cycles, buf, buf + 2);
+    cudaEventRecord(b);
+    if (e == cudaSuccess) e = cudaEventSynchronize(b);
+    if (e == cudaSuccess) e = cudaMemcpy(host, buf, 2 * sizeof(uint32_t), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && host[1]) break;
+  }
+  if (e == cudaSuccess) {
+    float t = 0;
+    cudaEventElapsedTime(&t, a, b);
+    *ms = t;
+    unsigned long long c = 0;
+    e = cudaMemcpy(&c, cycles, sizeof(c), cudaMemcpyDeviceToHost);
+    *hop_cycles = static_cast<double>(c) / (2.0 * iters);
+    *timed_out = host[1] != 0;
+  }
+  cudaEventDestroy(a);
+  cudaEventDestroy(b);
+  cudaFree(cycles);
+  cudaFree(buf);
+  return e;
 }
 
 template <int kKind>
@@ -150,6 +249,18 @@ extern "C" int dsmem_hist_microbench(int32_t kind, int32_t cluster_size, int32_t
     case DSMEM_HIST_MB_CLUSTER_BARRIER:
       e = dsmh::run_probe<DSMEM_HIST_MB_CLUSTER_BARRIER>(cluster_size, iters, value, ms);
       break;
+    case DSMEM_HIST_MB_DSMEM_PINGPONG:
+    case DSMEM_HIST_MB_GMEM_PINGPONG: {
+      if (cluster_size < 2 || iters > (1 << 20))
+        return dsmh::record_error(DSMEM_HIST_EINVAL, "microbench: ping-pong needs cluster_size >= 2, iters <= 2^20");
+      bool timed_out = false;
+      e = kind == DSMEM_HIST_MB_DSMEM_PINGPONG
+              ? dsmh::run_pingpong<false>(cluster_size, iters, value, ms, &timed_out)
+              : dsmh::run_pingpong<true>(cluster_size, iters, value, ms, &timed_out);
+      if (e == cudaSuccess && timed_out)
+        return dsmh::record_error(DSMEM_HIST_ETIMEOUT, "microbench: ping-pong peer did not answer");
+      break;
+    }
     default:
       return dsmh::record_error(DSMEM_HIST_EINVAL, "microbench: unknown kind");
   }

@@ -163,6 +163,24 @@ __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t cta_addr) {
 __device__ __forceinline__ void st_shared_u16(uint32_t cta_addr, uint16_t v) {
   asm volatile("st.shared.u16 [%0], %1;" ::"r"(cta_addr), "h"(v));
 }
+// Release stores and acquire loads for flag passing between CTAs.
+__device__ __forceinline__ void st_release_cluster(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.release.cluster.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_cluster(uint32_t cta_addr) {
+  uint32_t v;
+  asm volatile("ld.acquire.cluster.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(cta_addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ int4 ld_stream_v4(const int4* p) {
   int4 v;
   asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.s32 {%0, %1, %2, %3}, [%4];"

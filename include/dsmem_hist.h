@@ -219,18 +219,28 @@ enum {
   DSMEM_HIST_MB_REMOTE_RED = 1,            /* red.shared::cluster.add.u32 into a peer's slice */
   DSMEM_HIST_MB_REMOTE_ST16_SCATTERED = 2, /* st.shared::cluster.v4, random peer and address */
   DSMEM_HIST_MB_REMOTE_ST16_COALESCED = 3, /* st.shared::cluster.v4, 512 contiguous bytes per warp */
-  DSMEM_HIST_MB_CLUSTER_BARRIER = 4        /* barrier.cluster arrive + wait */
+  DSMEM_HIST_MB_CLUSTER_BARRIER = 4,       /* barrier.cluster arrive + wait */
+  DSMEM_HIST_MB_DSMEM_PINGPONG = 5,        /* one-way latency of a flag in a peer CTA's shared memory */
+  DSMEM_HIST_MB_GMEM_PINGPONG = 6          /* one-way latency of a flag in global memory */
 };
 
 /* Measures one DSMEM primitive on the current GPU ("Hopper DSMEM vs HBM",
- * tile-exchange and ping-pong sections; "CREDIT", microbenchmark section):
- * 1024 threads per CTA, 128 KiB of shared memory per CTA, every resident
- * cluster of `cluster_size` CTAs, `iters` operations per thread.
+ * tile-exchange and ping-pong sections; "CREDIT", microbenchmark section).
+ * Rate kinds (0..4): 1024 threads per CTA, 128 KiB of shared memory per CTA,
+ * every resident cluster of `cluster_size` CTAs, `iters` operations per
+ * thread.  Ping-pong kinds (5, 6): one cluster of `cluster_size` >= 2 CTAs;
+ * one thread of CTA 0 and one of CTA 1 pass a counter back and forth `iters`
+ * times through a flag in the receiver's shared memory (written with a
+ * release store to shared::cluster, read with acquire loads) or in global
+ * memory (release/acquire at GPU scope), as the page's ping-pong test does.
+ * Every wait for the peer is bounded (2^20 polls); a wait that gives up ends
+ * the test with DSMEM_HIST_ETIMEOUT.
  *   *value  operations per clock per SM (bytes per clock per SM for the two
- *           store kinds; clock cycles per barrier for the barrier kind)
+ *           store kinds; clock cycles per barrier for the barrier kind;
+ *           clock cycles per one-way hop, half a round trip, for ping-pong)
  *   *ms     wall time of the timed launch
  * Synchronous; allocates and frees its own small device buffers.  With
- * cluster_size 1 the "remote" kinds address this CTA itself. */
+ * cluster_size 1 the "remote" rate kinds address this CTA itself. */
 DSMEM_HIST_API int dsmem_hist_microbench(int32_t kind, int32_t cluster_size, int32_t iters,
                                          double* value, double* ms);
 

@@ -213,6 +213,10 @@ def test_tune_and_microbench_reject_bad_arguments():
     v, ms = ctypes.c_double(), ctypes.c_double()
     assert L.dsmem_hist_microbench(0, 17, 16, ctypes.byref(v), ctypes.byref(ms)) == pkg.DSMEM_HIST_EINVAL
     assert L.dsmem_hist_microbench(0, 2, 0, ctypes.byref(v), ctypes.byref(ms)) == pkg.DSMEM_HIST_EINVAL
+    # ping-pong needs two CTAs and a bounded number of rounds
+    assert L.dsmem_hist_microbench(5, 1, 16, ctypes.byref(v), ctypes.byref(ms)) == pkg.DSMEM_HIST_EINVAL
+    assert L.dsmem_hist_microbench(6, 2, (1 << 20) + 1, ctypes.byref(v), ctypes.byref(ms)) == \
+        pkg.DSMEM_HIST_EINVAL
 
 
 def test_ship_threads_match_header():

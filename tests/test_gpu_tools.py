@@ -46,6 +46,11 @@ def test_tune_ranks_every_shape_and_its_winner_is_exact(num_bins):
 def test_microbench_rates_are_consistent():
     rates = {k: pkg.dsmem_hist_microbench(k, 2, iters=512)
              for k in pkg.MICROBENCH_KINDS}
+    # one-way flag latency: hundreds to thousands of cycles, and a flag in a
+    # peer's shared memory arrives no later than one in global memory
+    for k in ("dsmem_pingpong", "gmem_pingpong"):
+        assert 20 < rates[k]["value"] < 1e5, rates[k]
+    assert rates["dsmem_pingpong"]["value"] < 1.5 * rates["gmem_pingpong"]["value"]
     for r in rates.values():
         assert r["value"] > 0 and r["ms"] > 0
     # a local shared-memory atomic is far cheaper than a remote one
