@@ -19,6 +19,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -206,6 +207,30 @@ def kernel_traffic(n_keys, num_bins, cluster_size, kernel_id):
     return None
 
 
+ARM_PARTS = {"0xd4f": "Arm Neoverse V2", "0xd40": "Arm Neoverse V1", "0xd49": "Arm Neoverse N2",
+             "0xd0c": "Arm Neoverse N1"}
+
+
+def host_info():
+    """The host the CPU baseline ran on: logical CPUs and the CPU model."""
+    model = platform.processor() or platform.machine()
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip().lower(), v.strip())
+    except OSError:
+        pass
+    if "model name" in fields:
+        model = fields["model name"]
+    elif "cpu part" in fields:
+        part = fields["cpu part"].lower()
+        model = ARM_PARTS.get(part, f"Arm CPU part {part}") + f" ({platform.machine()})"
+    return {"host_cpus": os.cpu_count(), "cpu_model": model}
+
+
 # ---------------------------------------------------------------- multi-rank
 
 def replica_seed(seed, rank):
@@ -266,7 +291,7 @@ def run_reference(a, world, rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
         "data": "synthetic (seeded generator)", "config": cfg,
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": desc},
+                         "sample": desc, **host_info()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -323,7 +348,8 @@ def run_ours(a, world, rank, local):
         parity = "bit-exact vs oracle" if np.array_equal(got, want) else \
             f"MISMATCH in {int((got != want).sum())} bins"
         cpu = {"value": n / med, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"full {n}-key workload (seed {seed}), median of {reps} runs"}
+               "sample": f"full {n}-key workload (seed {seed}), median of {reps} runs",
+               **host_info()}
 
     sampler = ClockSampler(gpu_id_for(torch, local))
     sampler.start()
