@@ -290,7 +290,7 @@ int check_plan(const DeviceState* st, const dsmem_hist_plan_t* p, int32_t num_bi
   if (p->kernel == DSMEM_HIST_KERNEL_SHIP) {
     const int nq = p->sub_vectors;
     if (P < 2 || p->block_threads != kShipThreads || (p->keys_per_thread != 4 && p->keys_per_thread != 8) ||
-        nq < 1 || nq > 32 || S + 32 >= 0xFFFF ||
+        nq < 1 || nq > 4096 || S + 32 >= 0xFFFF ||
         p->smem_bytes != 4 * S + static_cast<int64_t>(ship_staging_bytes(static_cast<int>(P), nq)))
       return fail(DSMEM_HIST_EINVAL, "plan: ship kernel fields inconsistent");
   } else if (p->kernel != DSMEM_HIST_KERNEL_DIRECT || p->smem_bytes != 4 * S) {

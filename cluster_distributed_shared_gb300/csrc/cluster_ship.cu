@@ -216,24 +216,26 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
   c.magic = a.magic;
   const uint32_t P = c.P;
   c.PS = P * a.S;
-  const uint32_t qs = 8u * a.sub_vectors;  // rows of an owner block
+  const uint32_t qs = a.sub_vectors;  // rows of an owner block
   c.blk = 64u * qs;
   const uint32_t cid = cluster_id_x();
 
   // Layout (must match ship_staging_bytes): slice u32[S + 32], cursors
-  // u32[2][P + 1][32], headers u32[2][16], sink u16[32], two inbox
-  // mbarriers (256 bytes with padding), staging u16[P][qs][32], inboxes
-  // u16[2][P][qs][32].
+  // u32[3][P + 1][32], headers u32[2][16], sink u16[32], two inbox
+  // mbarriers (256 bytes with padding), staging u16[2][P][qs][32], inboxes
+  // u16[2][P][qs][32].  Round r partitions into staging buffer r % 2 with
+  // cursor set r % 3, and its blocks travel in inbox buffer r % 2.
   const uint32_t sbase = smem_u32(smem);
   c.slice = sbase;
+  const uint32_t set_words = 32u * (P + 1u);
+  const uint32_t set_bytes = 4u * set_words;
   const uint32_t cur0 = sbase + 4u * (a.S + 32u);
-  const uint32_t header0 = cur0 + 256u * (P + 1u);
+  const uint32_t header0 = cur0 + 3u * set_bytes;
   c.sink = header0 + 128u + 2u * c.lane;
   const uint32_t full0 = header0 + 192u;  // mbarriers full[2]: inbox buffer complete
   const uint32_t stage0 = header0 + 256u;
-  const uint32_t inbox0 = stage0 + P * c.blk;
-  c.lim0 = stage0 + c.blk;
-  uint32_t* cursor = reinterpret_cast<uint32_t*>(smem + (cur0 - sbase));
+  const uint32_t buf_bytes = P * c.blk;   // one staging or inbox buffer
+  const uint32_t inbox0 = stage0 + 2u * buf_bytes;
 
   // Key stream: warp tiles of 32 vectors (tile t = vectors 32t .. 32t+31),
   // kKpt/4 tiles per warp per round; tile indices fit 32 bits (n < 2^39).
@@ -248,29 +250,28 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
 
   // Ship and apply: warp w serves owner (and sender) w mod P, as member sg of
   // the sng warps that do; lane l of member sg starts at vector 32*sg + l of
-  // a block and steps by 32*sng vectors.  Every address below is for buffer
-  // (or cursor set) 0; buffer 1 adds a fixed offset.
+  // a block and steps by 32*sng vectors.  Addresses below are for buffer 0;
+  // buffer 1 adds buf_bytes.
   const uint32_t so = warp % P;
   const uint32_t sg = warp / P;
   const uint32_t sng = (kWarps - 1u - so) / P + 1u;
   const uint32_t step = 512u * sng;                          // bytes between a lane's vectors
   const uint32_t vofs = 16u * (32u * sg + c.lane);           // this lane's first vector
-  const uint32_t set_words = 32u * (P + 1u);
-  const uint32_t set_bytes = 4u * set_words;
-  const uint32_t buf_bytes = P * c.blk;                      // one inbox buffer
-  const uint32_t top = stage0 + so * c.blk;                  // owner so's staging block
-  const uint32_t fill_rd = cur0 + 4u * (32u * so + c.lane);  // cursor (so, lane)
-  const uint32_t col_top = top + 2u * c.lane;                // its initial value
+  const uint32_t top0 = stage0 + so * c.blk;                 // owner so's staging block
+  const uint32_t fill_rd = cur0 + 4u * (32u * so + c.lane);  // cursor (so, lane) of set 0
   const uint32_t hdr_out = map_rank(header0 + 4u * rank, so);
   const uint32_t dst0 = map_rank(inbox0 + rank * c.blk, so) + vofs;
   const uint32_t src0 = inbox0 + so * c.blk + vofs;
   const uint32_t hdr_in = header0 + 4u * so;
   const uint32_t full_out = map_rank(full0, so);
+  const uint32_t cur_lane0 = cur0 + 4u * c.lane;
   // Cursor reset: thread i < set_words owns word i of a set.
   const uint32_t rs_row = threadIdx.x >> 5;
-  const uint32_t rs_val = rs_row < P ? stage0 + rs_row * c.blk + 2u * c.lane : kAlwaysFull;
   const uint32_t rs_addr = cur0 + 4u * threadIdx.x;
   const bool resets = threadIdx.x < set_words;
+  auto reset_value = [&](uint32_t b) {
+    return rs_row < P ? stage0 + b * buf_bytes + rs_row * c.blk + 2u * c.lane : kAlwaysFull;
+  };
 
   // Padding of this lane: it only ever touches vectors v with v mod 4 ==
   // lane mod 4, i.e. columns 8*(lane mod 4) .. +7.
@@ -285,10 +286,10 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
 
     uint4* s4 = reinterpret_cast<uint4*>(smem);
     for (uint32_t i = threadIdx.x; i < (c.S + 32u) / 4; i += blockDim.x) s4[i] = make_uint4(0, 0, 0, 0);
-    for (uint32_t v = threadIdx.x; v < 4u * qs * P; v += blockDim.x) st_shared_v4(stage0 + 16u * v, pad);
-    for (uint32_t i = threadIdx.x; i < 2u * set_words; i += blockDim.x) {
-      const uint32_t o = (i % set_words) >> 5;
-      cursor[i] = o < P ? stage0 + o * c.blk + 2u * (i & 31u) : kAlwaysFull;
+    for (uint32_t v = threadIdx.x; v < 8u * qs * P; v += blockDim.x) st_shared_v4(stage0 + 16u * v, pad);
+    if (resets) {
+      st_shared_u32(rs_addr, reset_value(0));              // set 0: round 0, buffer 0
+      st_shared_u32(rs_addr + set_bytes, reset_value(1));  // set 1: round 1, buffer 1
     }
     if (threadIdx.x < 32u) st_shared_u32(header0 + 4u * threadIdx.x, 0u);
     if (threadIdx.x == 0) {
@@ -302,52 +303,62 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
     int4 cur[kTiles];
     if (rounds > 0) {
       load_round<kKpt>(cur, vec, ntiles, gwarp, nwarps, rounds == 1);
-      c.cur_lane = cur0 + 4u * c.lane;
+      c.cur_lane = cur_lane0;
+      c.lim0 = stage0 + c.blk;
       partition_round<kTiles, kPow2>(cur, c);
+      if (rounds > 1) load_round<kKpt>(cur, vec, ntiles, gwarp + per_round, nwarps, rounds == 2);
     }
+    __syncthreads();  // round 0 staged
+    uint32_t k = 0;  // r % 3
     for (uint32_t r = 0; r < rounds; ++r) {
-      const bool more = r + 1 < rounds;
-      if (more) load_round<kKpt>(cur, vec, ntiles, gwarp + (r + 1) * per_round, nwarps, r + 2 == rounds);
-      const uint32_t buf = r & 1u;
-      // The cluster barrier's arrivals precede the partition, so only this
-      // barrier orders the partition before the ship.
-      __syncthreads();  // round r staged
+      const uint32_t b = r & 1u;
       {
-        // Ship owner so's block of this round: rows = its fullest column.
-        const uint32_t fill = (ld_shared_u32(fill_rd + buf * set_bytes) - col_top) >> 6;
+        // Ship owner so's block of round r: rows = its fullest column.
+        const uint32_t top = top0 + b * buf_bytes;
+        const uint32_t fill = (ld_shared_u32(fill_rd + k * set_bytes) - (top + 2u * c.lane)) >> 6;
         const uint32_t rows = __reduce_max_sync(kFullMask, min(fill, qs));
-        const uint32_t mbar = full_out + 8u * buf;
+        const uint32_t mbar = full_out + 8u * b;
         if (sg == 0 && c.lane == 0) {
           mbar_arrive_expect_tx_remote(mbar, 64u * rows + 4u);
-          st_async_u32(hdr_out + 64u * buf, rows, mbar);
+          st_async_u32(hdr_out + 64u * b, rows, mbar);
         }
         const uint32_t end = top + 64u * rows;
-        for (uint32_t at = top + vofs, dt = dst0 + buf * buf_bytes; at < end; at += step, dt += step) {
+        for (uint32_t at = top + vofs, dt = dst0 + b * buf_bytes; at < end; at += step, dt += step) {
           st_async_v4(dt, ld_shared_v4(at), mbar);
           st_shared_v4(at, pad);
         }
       }
       if (r > 0) {
-        // Apply sender so's block of the previous round, once every sender
-        // has arrived and every byte has landed.
-        const uint32_t pb = buf ^ 1u;
+        // Apply sender so's block of round r - 1, once every sender has
+        // arrived and every byte has landed.
+        const uint32_t pb = b ^ 1u;
         if (wait_inbox(full0 + 8u * pb, ((r - 1u) >> 1) & 1u)) {
           const uint32_t src = src0 + pb * buf_bytes;
           const uint32_t end = src - vofs + 64u * min(ld_shared_u32(hdr_in + 64u * pb), qs);
           for (uint32_t at = src; at < end; at += step) apply_vector(c.slice, ld_shared_v4(at));
         }
       }
-      __syncthreads();  // staging shipped and re-padded; this round's cursors read
-      if (resets) st_shared_u32(rs_addr + buf * set_bytes, rs_val);
+      // Set (r + 2) % 3 was last read by round r - 1's ship; round r + 2
+      // partitions with it into buffer b.
+      const uint32_t k2 = k == 0 ? 2u : k - 1u;
+      if (resets) st_shared_u32(rs_addr + k2 * set_bytes, reset_value(b));
       // Relaxed: inbox data is published through the mbarriers; this
       // barrier only tells senders that round r-1's inbox has been read
       // (every load of it has returned: its values fed the reds above).
       cluster_arrive_relaxed();
-      if (more) {
-        c.cur_lane = cur0 + 4u * c.lane + (buf ^ 1u) * set_bytes;
+      const uint32_t k1 = k == 2 ? 0u : k + 1u;
+      if (r + 1 < rounds) {
+        // Partition round r + 1 into the other buffer while other warps
+        // still ship and apply round r; then load round r + 2.
+        c.cur_lane = cur_lane0 + k1 * set_bytes;
+        c.lim0 = stage0 + (b ^ 1u) * buf_bytes + c.blk;
         partition_round<kTiles, kPow2>(cur, c);
+        if (r + 2 < rounds)
+          load_round<kKpt>(cur, vec, ntiles, gwarp + (r + 2) * per_round, nwarps, r + 3 == rounds);
       }
-      cluster_wait();  // round r's inboxes complete everywhere; round r+1 staged
+      cluster_wait();   // round r's inboxes complete everywhere
+      __syncthreads();  // round r + 1 staged; round r's staging and cursors read
+      k = k1;
     }
     if (rounds > 0) {
       const uint32_t pb = (rounds - 1u) & 1u;

@@ -39,7 +39,7 @@ struct ClusterHistArgs {
   uint64_t stride;      // partial row stride (u32 elements, multiple of 4)
   uint32_t head;        // keys before the first 16-byte boundary of `keys` (0..3, <= n)
   uint32_t accumulate;  // 1: add the slice into the partial row, 0: overwrite it
-  uint32_t sub_vectors; // ship kernel: 16-byte vectors per sub-bucket (power of two)
+  uint32_t sub_vectors; // ship kernel: rows of each owner's staging block
 };
 
 // Launches (all asynchronous on `stream`).
@@ -55,7 +55,7 @@ cudaError_t launch_cluster_control(const dsmem_hist_plan_t& plan, uint32_t* sink
                                    cudaStream_t stream);
 
 // Ship kernel (cluster_ship.cu; its staging size is computed by the planner).
-uint32_t ship_staging_bytes(int cluster_size, int sub_vectors);
+uint32_t ship_staging_bytes(int cluster_size, int rows);
 cudaError_t prepare_ship_kernel(int keys_per_thread, int smem_bytes);
 cudaError_t query_ship_active_clusters(int keys_per_thread, int cluster_size, int smem_bytes,
                                        int* out);

@@ -16,8 +16,9 @@
 //             a few never-hit counters instead, and no bin is dropped)
 //   kernel  = SHIP (keys shipped to owners as 16-bit indices, local atomics)
 //             when P >= 2 and the slice plus its staging fit one CTA: 8 keys
-//             per thread per round if that fits, else 4, with sub-buckets
-//             holding twice (else 1.5 times) the expected entries; else DIRECT
+//             per thread per round if that fits, else 4, with staging rows
+//             holding twice the expected entries per column (at least 1.5
+//             times); else DIRECT
 //   threads = 1024 for SHIP; for DIRECT 1024 when only one CTA fits an SM,
 //             else 512
 //   C       = min(resident clusters, clusters needed so each CTA gets at
@@ -32,13 +33,13 @@ namespace dsmh {
 uint64_t owner_magic(uint32_t S) { return ((uint64_t{1} << 40) / S) + 1; }
 
 // Shared memory the ship kernel needs beside the slice; the kernel lays it
-// out in this order: 32 padding counters after the slice, two cursor sets
-// u32[P + 1][32], inbox headers u32[2][16] plus a 16-bit sink per lane (256
-// bytes in all), the staging blocks u16[P][qs][32] and the inboxes
-// u16[2][P][qs][32] (qs = 8 * sub_vectors rows of 64 bytes).
-uint32_t ship_staging_bytes(int cluster_size, int sub_vectors) {
-  const uint32_t P = static_cast<uint32_t>(cluster_size), nq = static_cast<uint32_t>(sub_vectors);
-  return 4u * 32u + 8u * 32u * (P + 1u) + 256u + 3u * P * 64u * 8u * nq;
+// out in this order: 32 padding counters after the slice, three cursor sets
+// u32[P + 1][32], inbox headers u32[2][16] plus a 16-bit sink per lane and
+// two mbarriers (256 bytes), then two staging buffers and two inbox buffers
+// of P blocks of `rows` rows of 64 bytes.
+uint32_t ship_staging_bytes(int cluster_size, int rows) {
+  const uint32_t P = static_cast<uint32_t>(cluster_size), q = static_cast<uint32_t>(rows);
+  return 4u * 32u + 3u * 4u * 32u * (P + 1u) + 256u + 4u * P * 64u * q;
 }
 
 static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -118,20 +119,23 @@ int plan_shape(const dsmem_hist_device_t* dev, int32_t num_bins, int64_t n,
         return DSMEM_HIST_EINVAL;
       }
     } else {
-      // Sub-bucket capacity: twice the expected 32*k/P entries per round, else
-      // 1.5 times (rounded up to whole 8-entry vectors); 8 keys per thread and
-      // round before 4.
-      for (int t = 0; t < 4 && !kernel; ++t) {
-        const int k = t < 2 ? 8 : 4;
-        const int64_t expect = (kShipThreads / 32) * k;  // entries per column per round, times P
-        const int q = static_cast<int>(ceil_div((t % 2 == 0 ? 2 * expect : 3 * expect / 2), 8 * P));
-        const int64_t need = 4 * S + ship_staging_bytes(P, q);
-        if (need <= dev->max_smem_per_block_optin &&
-            need + kSmemReservedPerCta <= dev->max_smem_per_sm) {
+      // Staging rows per owner block: twice the expected entries per column
+      // and round, or as many as fit down to 1.5 times; 8 keys per thread
+      // and round before 4.
+      for (int k = 8; k >= 4 && !kernel; k -= 4) {
+        const int64_t expect = static_cast<int64_t>(kShipThreads / 32) * k;  // per column and round, times P
+        const int64_t want = ceil_div(2 * expect, P), least = ceil_div(3 * expect, 2 * P);
+        const int64_t room = static_cast<int64_t>(dev->max_smem_per_block_optin) - 4 * S -
+                             ship_staging_bytes(P, 0);
+        const int64_t room_sm = static_cast<int64_t>(dev->max_smem_per_sm) - kSmemReservedPerCta - 4 * S -
+                                ship_staging_bytes(P, 0);
+        const int64_t fit = (room < room_sm ? room : room_sm) / (4 * 64 * P);
+        const int64_t q = want < fit ? want : fit;
+        if (q >= least && q >= 1) {
           kernel = DSMEM_HIST_KERNEL_SHIP;
           kpt = k;
-          nq = q;
-          smem = static_cast<int>(need);
+          nq = static_cast<int>(q);
+          smem = static_cast<int>(4 * S + ship_staging_bytes(P, nq));
         }
       }
       if (!kernel && req->kernel == DSMEM_HIST_KERNEL_SHIP) {

@@ -80,8 +80,8 @@ typedef struct dsmem_hist_plan {
   int32_t max_active_clusters; /* occupancy answer for this shape (0 when not queried) */
   int32_t kernel;              /* DSMEM_HIST_KERNEL_DIRECT or DSMEM_HIST_KERNEL_SHIP */
   int32_t keys_per_thread;     /* ship kernel: keys each thread partitions per round (4 or 8) */
-  int32_t sub_vectors;         /* ship kernel: rows of each owner's staging block, in units
-                                  of 8 (each row: 32 columns of 16-bit entries) */
+  int32_t sub_vectors;         /* ship kernel: rows of each owner's staging block (each row:
+                                  32 columns of 16-bit entries) */
   int32_t reserved;            /* zero */
   int64_t partial_stride;      /* u32 elements between two clusters' partial rows (num_bins rounded up to 4) */
   int64_t workspace_bytes;     /* scratch: num_clusters * partial_stride * 4 */

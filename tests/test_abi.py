@@ -109,8 +109,8 @@ def test_planner_covers_every_bin(nb, slice_cap):
         if p["kernel"] == pkg.KERNEL_SHIP:
             assert P >= 2 and p["block_threads"] == pkg.SHIP_THREADS
             assert p["keys_per_thread"] in (4, 8)
-            nq = p["sub_vectors"]
-            assert nq >= 1 and 8 * nq * 32 * P >= 1.5 * pkg.SHIP_THREADS * p["keys_per_thread"]
+            nq = p["sub_vectors"]   # staging rows per owner block
+            assert nq >= 1 and nq * 32 * P >= 1.5 * pkg.SHIP_THREADS * p["keys_per_thread"]
             assert p["smem_bytes"] == 4 * S + ship_staging(P, nq)
             assert S < 0xFFFF                               # 16-bit local indices + sentinel
         else:
@@ -119,11 +119,11 @@ def test_planner_covers_every_bin(nb, slice_cap):
             assert P == forced
 
 
-def ship_staging(P, nq):
-    # padding counters, two cursor sets of P + 1 rows, headers + sink,
-    # staging blocks and two inboxes of 8 * nq rows of 64 bytes per owner
-    rows = 8 * nq
-    return 4 * 32 + 2 * 4 * 32 * (P + 1) + 256 + 3 * P * rows * 64
+def ship_staging(P, rows):
+    # padding counters, three cursor sets of P + 1 rows, headers + sink +
+    # mbarriers, two staging and two inbox buffers of P blocks of `rows`
+    # rows of 64 bytes
+    return 4 * 32 + 3 * 4 * 32 * (P + 1) + 256 + 4 * P * rows * 64
 
 
 @pytest.mark.parametrize("P", range(2, 17))
@@ -134,7 +134,7 @@ def test_ship_plan_fits_for_every_cluster_size(P):
         assert p["smem_bytes"] + 1024 <= GB300["max_smem_per_sm"]
         # staging columns hold at least 1.5 times the expected keys per (owner, lane) and round
         expected = pkg.SHIP_THREADS // 32 * p["keys_per_thread"] / P
-        assert 8 * p["sub_vectors"] >= 1.5 * expected
+        assert p["sub_vectors"] >= 1.5 * expected
 
 
 def test_owner_magic_exact():
