@@ -312,22 +312,6 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
     uint32_t k = 0;  // r % 3
     for (uint32_t r = 0; r < rounds; ++r) {
       const uint32_t b = r & 1u;
-      {
-        // Ship owner so's block of round r: rows = its fullest column.
-        const uint32_t top = top0 + b * buf_bytes;
-        const uint32_t fill = (ld_shared_u32(fill_rd + k * set_bytes) - (top + 2u * c.lane)) >> 6;
-        const uint32_t rows = __reduce_max_sync(kFullMask, min(fill, qs));
-        const uint32_t mbar = full_out + 8u * b;
-        if (sg == 0 && c.lane == 0) {
-          mbar_arrive_expect_tx_remote(mbar, 64u * rows + 4u);
-          st_async_u32(hdr_out + 64u * b, rows, mbar);
-        }
-        const uint32_t end = top + 64u * rows;
-        for (uint32_t at = top + vofs, dt = dst0 + b * buf_bytes; at < end; at += step, dt += step) {
-          st_async_v4(dt, ld_shared_v4(at), mbar);
-          st_shared_v4(at, pad);
-        }
-      }
       if (r > 0) {
         // Apply sender so's block of round r - 1, once every sender has
         // arrived and every byte has landed.
@@ -346,6 +330,22 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
       // barrier only tells senders that round r-1's inbox has been read
       // (every load of it has returned: its values fed the reds above).
       cluster_arrive_relaxed();
+      {
+        // Ship owner so's block of round r: rows = its fullest column.
+        const uint32_t top = top0 + b * buf_bytes;
+        const uint32_t fill = (ld_shared_u32(fill_rd + k * set_bytes) - (top + 2u * c.lane)) >> 6;
+        const uint32_t rows = __reduce_max_sync(kFullMask, min(fill, qs));
+        const uint32_t mbar = full_out + 8u * b;
+        if (sg == 0 && c.lane == 0) {
+          mbar_arrive_expect_tx_remote(mbar, 64u * rows + 4u);
+          st_async_u32(hdr_out + 64u * b, rows, mbar);
+        }
+        const uint32_t end = top + 64u * rows;
+        for (uint32_t at = top + vofs, dt = dst0 + b * buf_bytes; at < end; at += step, dt += step) {
+          st_async_v4(dt, ld_shared_v4(at), mbar);
+          st_shared_v4(at, pad);
+        }
+      }
       const uint32_t k1 = k == 2 ? 0u : k + 1u;
       if (r + 1 < rounds) {
         // Partition round r + 1 into the other buffer while other warps
