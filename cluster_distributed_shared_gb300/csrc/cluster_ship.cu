@@ -269,9 +269,8 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
   const uint32_t rs_row = threadIdx.x >> 5;
   const uint32_t rs_addr = cur0 + 4u * threadIdx.x;
   const bool resets = threadIdx.x < set_words;
-  auto reset_value = [&](uint32_t b) {
-    return rs_row < P ? stage0 + b * buf_bytes + rs_row * c.blk + 2u * c.lane : kAlwaysFull;
-  };
+  const uint32_t rs_val0 = rs_row < P ? stage0 + rs_row * c.blk + 2u * c.lane : kAlwaysFull;
+  const uint32_t rs_val1 = rs_row < P ? rs_val0 + buf_bytes : kAlwaysFull;
 
   // Padding of this lane: it only ever touches vectors v with v mod 4 ==
   // lane mod 4, i.e. columns 8*(lane mod 4) .. +7.
@@ -288,8 +287,8 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
     for (uint32_t i = threadIdx.x; i < (c.S + 32u) / 4; i += blockDim.x) s4[i] = make_uint4(0, 0, 0, 0);
     for (uint32_t v = threadIdx.x; v < 8u * qs * P; v += blockDim.x) st_shared_v4(stage0 + 16u * v, pad);
     if (resets) {
-      st_shared_u32(rs_addr, reset_value(0));              // set 0: round 0, buffer 0
-      st_shared_u32(rs_addr + set_bytes, reset_value(1));  // set 1: round 1, buffer 1
+      st_shared_u32(rs_addr, rs_val0);              // set 0: round 0, buffer 0
+      st_shared_u32(rs_addr + set_bytes, rs_val1);  // set 1: round 1, buffer 1
     }
     if (threadIdx.x < 32u) st_shared_u32(header0 + 4u * threadIdx.x, 0u);
     if (threadIdx.x == 0) {
@@ -325,7 +324,7 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
       // Set (r + 2) % 3 was last read by round r - 1's ship; round r + 2
       // partitions with it into buffer b.
       const uint32_t k2 = k == 0 ? 2u : k - 1u;
-      if (resets) st_shared_u32(rs_addr + k2 * set_bytes, reset_value(b));
+      if (resets) st_shared_u32(rs_addr + k2 * set_bytes, b ? rs_val1 : rs_val0);
       // Relaxed: inbox data is published through the mbarriers; this
       // barrier only tells senders that round r-1's inbox has been read
       // (every load of it has returned: its values fed the reds above).
