@@ -109,7 +109,7 @@ int plan_shape(const dsmem_hist_device_t* dev, int32_t num_bins, int64_t n,
     return DSMEM_HIST_EINVAL;
   }
   // Kernel choice: shipping whenever the cluster has remote owners and its
-  // staging fits beside the slice (1024 threads), else direct increments.
+  // staging fits beside the slice (kShipThreads threads), else direct increments.
   int kernel = DSMEM_HIST_KERNEL_DIRECT, kpt = 0, nq = 0;
   const bool ship_ok_threads = req->block_threads == 0 || req->block_threads == kShipThreads;
   if (req->kernel == DSMEM_HIST_KERNEL_SHIP || (req->kernel < 0 && P >= 2 && ship_ok_threads)) {

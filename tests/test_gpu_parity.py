@@ -133,7 +133,7 @@ def test_ragged_small_lengths(n):
 
 
 def test_ship_overflow_and_runs_paths():
-    # Keys that all belong to one owner overflow its sub-buckets (remote
+    # Keys that all belong to one owner overflow its staging columns (remote
     # increments take over); runs of equal keys take the whole-tile path;
     # partial runs and run boundaries mix both.
     rng = np.random.default_rng(3)
