@@ -106,10 +106,10 @@ __device__ __forceinline__ void stage_entry(uint32_t ea, uint32_t lim, uint32_t 
 // pass starts at bin 0, so a key is its own in-pass offset.
 template <bool kPow2, bool kBase0>
 __device__ __forceinline__ void partition_tile(const int4& v, const Ctx& c) {
-  const bool eq4 = (v.x == v.y) & (v.y == v.z) & (v.z == v.w);
-  if (__all_sync(kFullMask, eq4)) {  // rare on most inputs: then test the whole tile
+  if (__all_sync(kFullMask, v.x == v.w)) {  // rare on most inputs: then test the whole tile
     const int32_t k0 = __shfl_sync(kFullMask, v.x, 0);
-    if (__all_sync(kFullMask, v.x == k0)) {
+    const bool eq4 = (v.x == v.y) & (v.y == v.z) & (v.z == v.w);
+    if (__all_sync(kFullMask, eq4 & (v.x == k0))) {
       const uint32_t rel = static_cast<uint32_t>(k0) - (kBase0 ? 0u : c.base);
       if (c.lane == 0 && rel < c.range) {
         uint32_t o, loc;
