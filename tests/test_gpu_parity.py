@@ -302,3 +302,36 @@ def test_plan_on_device_confirms_cluster_16():
     p8 = pkg.dsmem_hist_plan(262144, 1 << 28)
     assert p8["cluster_size"] == 8 and p8["max_active_clusters"] >= 1
     assert p8["num_clusters"] == p8["max_active_clusters"]
+
+
+def test_randomized_shapes_and_inputs():
+    # Seeded random trials over bin counts, lengths, misaligned starts, forced
+    # cluster sizes and kernels, and key mixes (negatives, out of range,
+    # runs, one hot bin); every result bit-exact against the oracle.
+    rng = np.random.default_rng(2024)
+    for trial in range(60):
+        num_bins = int(rng.choice([1, 7, 100, 4096, 8191, 40000, 65536, 131072, 262144, 300007]))
+        n = int(rng.integers(0, 3_000_000))
+        off = int(rng.integers(0, 4))
+        keys = rng.integers(-num_bins // 8 - 2, num_bins + num_bins // 8 + 2, n + off).astype(np.int32)
+        if trial % 3 == 0 and n > 1024:                      # runs of equal keys
+            starts = rng.integers(0, n - 512, 16)
+            for s0 in starts:
+                keys[s0:s0 + 512] = rng.integers(0, num_bins)
+        if trial % 4 == 1 and n > 0:                         # one hot bin
+            keys[rng.random(n + off) < 0.2] = rng.integers(0, num_bins)
+        P = int(rng.choice([0, 2, 3, 4, 8, 16]))
+        kw = {}
+        if P:
+            kw["cluster_size"] = P
+        if P >= 2 and trial % 2 == 0:
+            kw["kernel"] = SH
+        elif P and trial % 5 == 0:
+            kw["kernel"] = D
+        sub = keys[off:off + n]
+        want = oracle.histogram(sub, num_bins)
+        dev = torch.from_numpy(keys).cuda()[off:off + n]
+        got = pkg.dsmem_hist(dev, num_bins, **kw)
+        torch.cuda.synchronize()
+        g = to_np(got)
+        assert np.array_equal(g, want), (trial, num_bins, n, off, kw, np.flatnonzero(g != want)[:8])
