@@ -166,18 +166,20 @@ __device__ __forceinline__ void apply_vector(uint32_t slice, const uint4& x) {
   red_add_local(__dp2a_lo(x.w, 0x400u, slice), 1u);
 }
 
-__device__ uint32_t g_ship_status;  // bit 0: a bounded wait gave up
+__device__ uint32_t g_ship_status;  // bit 0: a bounded wait gave up (until read and cleared)
 
 // Waits for phase `parity` of an inbox mbarrier, at most ~1e8 cycles
-// (~50 ms).  On a timeout the device status word records it and the caller
-// skips the buffer; once any wait has timed out, later waits give up after
-// one probe.
-__device__ __forceinline__ bool wait_inbox(uint32_t mbar, uint32_t parity) {
+// (~50 ms).  On a timeout the device status word records it, this CTA's
+// shared flag at `gave_up` is set, and the caller skips the buffer; once a wait of
+// this CTA has timed out, its later waits in the same launch give up after
+// one probe.  Later launches start with the flag clear.
+__device__ __forceinline__ bool wait_inbox(uint32_t mbar, uint32_t parity, uint32_t gave_up) {
   if (mbar_try_wait(mbar, parity)) return true;
-  if (*reinterpret_cast<volatile uint32_t*>(&g_ship_status) != 0u) return false;
+  if (ld_shared_u32(gave_up) != 0u) return false;
   const long long deadline = clock64() + 100000000ll;
   while (clock64() < deadline)
     if (mbar_try_wait(mbar, parity)) return true;
+  st_shared_u32(gave_up, 1u);
   atomicOr(&g_ship_status, 1u);
   return false;
 }
@@ -222,7 +224,7 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
 
   // Layout (must match ship_staging_bytes): slice u32[S + 32], cursors
   // u32[3][P + 1][32], headers u32[2][16], sink u16[32], two inbox
-  // mbarriers (256 bytes with padding), staging u16[2][P][qs][32], inboxes
+  // mbarriers and a timeout flag (256 bytes with padding), staging u16[2][P][qs][32], inboxes
   // u16[2][P][qs][32].  Round r partitions into staging buffer r % 2 with
   // cursor set r % 3, and its blocks travel in inbox buffer r % 2.
   const uint32_t sbase = smem_u32(smem);
@@ -233,6 +235,9 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
   const uint32_t header0 = cur0 + 3u * set_bytes;
   c.sink = header0 + 128u + 2u * c.lane;
   const uint32_t full0 = header0 + 192u;  // mbarriers full[2]: inbox buffer complete
+  // A bounded wait of this CTA timed out in this launch (cleared below, before
+  // the first cluster barrier, so before any wait).
+  const uint32_t gave_up = header0 + 208u;
   const uint32_t stage0 = header0 + 256u;
   const uint32_t buf_bytes = P * c.blk;   // one staging or inbox buffer
   const uint32_t inbox0 = stage0 + 2u * buf_bytes;
@@ -291,6 +296,7 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
       st_shared_u32(rs_addr + set_bytes, rs_val1);  // set 1: round 1, buffer 1
     }
     if (threadIdx.x < 32u) st_shared_u32(header0 + 4u * threadIdx.x, 0u);
+    if (threadIdx.x == 0) st_shared_u32(gave_up, 0u);
     if (threadIdx.x == 0) {
       // One arrival per sender and round; the senders' bytes complete it.
       mbar_init(full0, P);
@@ -315,7 +321,7 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
         // Apply sender so's block of round r - 1, once every sender has
         // arrived and every byte has landed.
         const uint32_t pb = b ^ 1u;
-        if (wait_inbox(full0 + 8u * pb, ((r - 1u) >> 1) & 1u)) {
+        if (wait_inbox(full0 + 8u * pb, ((r - 1u) >> 1) & 1u, gave_up)) {
           const uint32_t src = src0 + pb * buf_bytes;
           const uint32_t end = src - vofs + 64u * min(ld_shared_u32(hdr_in + 64u * pb), qs);
           for (uint32_t at = src; at < end; at += step) apply_vector(c.slice, ld_shared_v4(at));
@@ -361,7 +367,7 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
     }
     if (rounds > 0) {
       const uint32_t pb = (rounds - 1u) & 1u;
-      if (wait_inbox(full0 + 8u * pb, ((rounds - 1u) >> 1) & 1u)) {
+      if (wait_inbox(full0 + 8u * pb, ((rounds - 1u) >> 1) & 1u, gave_up)) {
         const uint32_t src = src0 + pb * buf_bytes;
         const uint32_t end = src - vofs + 64u * min(ld_shared_u32(hdr_in + 64u * pb), qs);
         for (uint32_t at = src; at < end; at += step) apply_vector(c.slice, ld_shared_v4(at));
