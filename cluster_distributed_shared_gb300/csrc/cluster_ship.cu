@@ -14,7 +14,8 @@
 // idea of "CREDIT", section on the clustered reduction-reuse schedule).
 //
 // Per CTA (kShipThreads threads), keys are processed in rounds of
-// kShipThreads * kKpt keys; every warp does every phase.
+// kShipThreads * kKpt keys.  Round r stages into staging buffer r % 2 with
+// cursor set r % 3 and travels in inbox buffer r % 2.
 //   Partition.  Owner o's staging block is column-major: rows of 64 bytes,
 //     column L (0..31) holding the keys that lane L of any warp routed to o.
 //     Cursor (o, L) is the byte address of the column's next free entry, so
@@ -25,29 +26,28 @@
 //     rounds); a key outside the pass's bins meets a cursor row that is
 //     always full and is dropped on the same path.  A warp tile of 128 equal
 //     keys becomes one remote red of 128 (pre-aggregation of runs).
-//   Ship (after a CTA barrier that ends the partition).  Warps serve owner
-//     w mod P: the block's row count is the fullest column's fill, and its
-//     rows go out as contiguous 16-byte `st.async` stores into the owner's
-//     inbox slot for this sender, then are overwritten with padding entries
-//     (column c pads with index S + c, one of 32 never-read counters after
-//     the slice).  The row count goes to the owner's header the same way.
-//     Each store's bytes are counted on the owner's mbarrier for that inbox
-//     buffer, on which every sender arrives once per round with its byte
-//     count (`mbarrier.arrive.expect_tx`).
-//   Apply.  The same warps wait (bounded) for the previous round's mbarrier
-//     phase, then apply that round's inbox block from sender w mod P: one
-//     `dp2a` turns a 16-bit entry into its counter's address, one local red
-//     increments it.
-//   After a CTA barrier, every warp arrives on the cluster barrier, partitions
-//   the next round, and waits.  Since the mbarriers publish the inbox data,
-//   this barrier is relaxed: it only tells senders that the inbox they are
-//   about to overwrite has been read, so no warp waits for its remote stores
-//   to be acknowledged.
-// Inboxes are double-buffered: a sender writes round r into buffer r%2 only
-// after the barrier of round r-1, which every owner arrives on only after it
-// has applied round r-2 from that buffer.  Cursor sets alternate by round, so
-// the set a round's ship reads is reset while the next round partitions with
-// the other set.
+//   Ship.  Warps serve owner w mod P: the block's row count is the fullest
+//     column's fill, and its rows go out as contiguous 16-byte `st.async`
+//     stores into the owner's inbox slot for this sender, then are
+//     overwritten with padding entries (column c pads with index S + c, one
+//     of 32 never-read counters after the slice).  The row count goes to the
+//     owner's header the same way.  Each store's bytes are counted on the
+//     owner's mbarrier for that inbox buffer, on which every sender arrives
+//     once per round with its byte count (`mbarrier.arrive.expect_tx`).
+//   Apply.  Warps wait (bounded) for a round's mbarrier phase, then apply
+//     that round's inbox block from sender w mod P: one `dp2a` turns a
+//     16-bit entry into its counter's address, one local red increments it.
+// In round r every warp applies round r-1, resets the cursor set of round
+// r+2, arrives on the cluster barrier, ships round r, partitions round r+1
+// into the other staging buffer and loads the keys of round r+2, then waits
+// on the cluster barrier and meets the other warps at the round's only CTA
+// barrier.  Warps that finish applying and shipping partition while others
+// still apply, so the phases overlap.  Since the mbarriers publish the inbox
+// data, the cluster barrier is relaxed: it only tells senders that the inbox
+// they are about to overwrite has been read, so no warp waits for its remote
+// stores to be acknowledged.  A sender writes round r into inbox buffer r%2
+// only after the barrier of round r-1, which every owner arrives on only
+// after it has applied round r-2 from that buffer.
 
 #include <cuda_runtime.h>
 #include <stdint.h>
