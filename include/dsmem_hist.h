@@ -245,7 +245,17 @@ DSMEM_HIST_API int dsmem_hist_microbench(int32_t kind, int32_t cluster_size, int
                                          double* value, double* ms);
 
 /* Plan for the current device (queries its properties and the occupancy of
- * the chosen shape).  `request` may be NULL. */
+ * the chosen shape).  `request` may be NULL.
+ *
+ * Every entry point that plans on the current device (dsmem_hist,
+ * dsmem_hist_ex, dsmem_hist_host, dsmem_hist_static, dsmem_hist_plan) reads
+ * these environment variables for the request fields the caller left to the
+ * planner: DSMEM_HIST_CLUSTER (cluster_size), DSMEM_HIST_BLOCK
+ * (block_threads), DSMEM_HIST_GRID (num_clusters), DSMEM_HIST_AGGREGATE
+ * (aggregate) and DSMEM_HIST_KERNEL (kernel).  DSMEM_HIST_TRACE=1 prints
+ * each plan to stderr.  A shape whose clusters cannot be resident falls back
+ * from the ship kernel to the direct one, then (unless the cluster size was
+ * forced) to smaller clusters. */
 DSMEM_HIST_API int dsmem_hist_plan(int32_t num_bins, int64_t n, const dsmem_hist_request_t* request,
                     dsmem_hist_plan_t* out);
 

@@ -335,3 +335,14 @@ def test_randomized_shapes_and_inputs():
         torch.cuda.synchronize()
         g = to_np(got)
         assert np.array_equal(g, want), (trial, num_bins, n, off, kw, np.flatnonzero(g != want)[:8])
+
+
+def test_environment_overrides_fill_open_request_fields(monkeypatch):
+    monkeypatch.setenv("DSMEM_HIST_KERNEL", "0")
+    monkeypatch.setenv("DSMEM_HIST_CLUSTER", "4")
+    p = pkg.dsmem_hist_plan(262144, 1 << 24)
+    assert p["kernel"] == D and p["cluster_size"] == 4
+    forced = pkg.dsmem_hist_plan(262144, 1 << 24, cluster_size=8, kernel=SH)
+    assert forced["kernel"] == SH and forced["cluster_size"] == 8   # explicit fields win
+    keys = gen.uniform(1 << 20, 262144, seed=12)
+    assert np.array_equal(gpu_hist(keys, 262144), oracle.histogram(keys, 262144))
