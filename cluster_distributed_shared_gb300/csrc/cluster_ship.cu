@@ -298,9 +298,9 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
     if (threadIdx.x < 32u) st_shared_u32(header0 + 4u * threadIdx.x, 0u);
     if (threadIdx.x == 0) st_shared_u32(gave_up, 0u);
     if (threadIdx.x == 0) {
-      // One arrival per sender and round; the senders' bytes complete it.
-      mbar_init(full0, P);
-      mbar_init(full0 + 8u, P);
+      // One arrival per other sender and round; their bytes complete it.
+      mbar_init(full0, P - 1u);
+      mbar_init(full0 + 8u, P - 1u);
       fence_mbar_init();
     }
     cluster_barrier();  // slices zeroed and mbarriers initialised cluster-wide
@@ -317,9 +317,10 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
     uint32_t k = 0;  // r % 3
     for (uint32_t r = 0; r < rounds; ++r) {
       const uint32_t b = r & 1u;
-      if (r > 0) {
+      if (r > 0 && so != rank) {
         // Apply sender so's block of round r - 1, once every sender has
-        // arrived and every byte has landed.
+        // arrived and every byte has landed (this CTA's own block was
+        // applied straight from staging when it was shipped).
         const uint32_t pb = b ^ 1u;
         if (wait_inbox(full0 + 8u * pb, ((r - 1u) >> 1) & 1u, gave_up)) {
           const uint32_t src = src0 + pb * buf_bytes;
@@ -340,15 +341,23 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
         const uint32_t top = top0 + b * buf_bytes;
         const uint32_t fill = (ld_shared_u32(fill_rd + k * set_bytes) - (top + 2u * c.lane)) >> 6;
         const uint32_t rows = __reduce_max_sync(kFullMask, min(fill, qs));
-        const uint32_t mbar = full_out + 8u * b;
-        if (sg == 0 && c.lane == 0) {
-          mbar_arrive_expect_tx_remote(mbar, 64u * rows + 4u);
-          st_async_u32(hdr_out + 64u * b, rows, mbar);
-        }
         const uint32_t end = top + 64u * rows;
-        for (uint32_t at = top + vofs, dt = dst0 + b * buf_bytes; at < end; at += step, dt += step) {
-          st_async_v4(dt, ld_shared_v4(at), mbar);
-          st_shared_v4(at, pad);
+        if (so == rank) {
+          // This CTA's own block: apply it here instead of shipping it.
+          for (uint32_t at = top + vofs; at < end; at += step) {
+            apply_vector(c.slice, ld_shared_v4(at));
+            st_shared_v4(at, pad);
+          }
+        } else {
+          const uint32_t mbar = full_out + 8u * b;
+          if (sg == 0 && c.lane == 0) {
+            mbar_arrive_expect_tx_remote(mbar, 64u * rows + 4u);
+            st_async_u32(hdr_out + 64u * b, rows, mbar);
+          }
+          for (uint32_t at = top + vofs, dt = dst0 + b * buf_bytes; at < end; at += step, dt += step) {
+            st_async_v4(dt, ld_shared_v4(at), mbar);
+            st_shared_v4(at, pad);
+          }
         }
       }
       const uint32_t k1 = k == 2 ? 0u : k + 1u;
@@ -365,7 +374,7 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
       __syncthreads();  // round r + 1 staged; round r's staging and cursors read
       k = k1;
     }
-    if (rounds > 0) {
+    if (rounds > 0 && so != rank) {
       const uint32_t pb = (rounds - 1u) & 1u;
       if (wait_inbox(full0 + 8u * pb, ((rounds - 1u) >> 1) & 1u, gave_up)) {
         const uint32_t src = src0 + pb * buf_bytes;
