@@ -377,6 +377,13 @@ def run_ours(a, world, rank, local):
     ms_total = ev_start.elapsed_time(ev_end)
     kernel_ms = [s.elapsed_time(e) for s, e in ev_k]
     cluster_ms = sum(kernel_ms) / len(kernel_ms)
+    launch_stats = {"median": statistics.median(kernel_ms), "min": min(kernel_ms),
+                    "max": max(kernel_ms)}
+    if parity is not None:
+        # The timed launches wrote `bins` too: check their result as well.
+        got = bins.cpu().numpy().view(np.uint32)
+        if not np.array_equal(got, want):
+            parity = f"MISMATCH after the timed launches in {int((got != want).sum())} bins"
     ms_total = max_over_ranks(ms_total, pg, dev)
     ms_step = ms_total / a.steps
     value = whole_job_rate(world, n, a.steps, ms_total)
@@ -433,7 +440,7 @@ def run_ours(a, world, rank, local):
                      "peak": peak, "peak_source": peak_src, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes": alg_bytes, "avg_launch_ms": cluster_ms,
-                     "share_of_step": cluster_ms / ms_step},
+                     "launch_ms": launch_stats, "share_of_step": cluster_ms / ms_step},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "global_atomic_comparison": comparison,
