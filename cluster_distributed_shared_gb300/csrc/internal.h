@@ -14,8 +14,11 @@ namespace dsmh {
 // 16-byte vectors of four int32 keys.
 constexpr int kVecPerThread = 4;
 constexpr int kKeysPerThreadStep = 4 * kVecPerThread;
-// The planner gives every CTA at least this many unrolled steps of work.
+// The planner gives every CTA of the direct kernel at least this many
+// unrolled steps of work, and every CTA of the ship kernel at least this many
+// rounds (kShipThreads * keys_per_thread keys each).
 constexpr int kMinStepsPerCta = 4;
+constexpr int kMinShipRoundsPerCta = 2;
 // Default cap on one CTA's counter slice: 128 KiB leaves room for a second
 // small allocation per SM while keeping the slice count at the published
 // cluster sizes (2 x 32768 bins, 8 x 32768, 16 x 32768).

@@ -22,8 +22,9 @@
 //   threads = kShipThreads (768) for SHIP; for DIRECT 1024 when only one CTA fits an SM,
 //             else 512
 //   C       = min(resident clusters, clusters needed so each CTA gets at
-//             least kMinStepsPerCta unrolled steps of keys, clusters whose
-//             partial rows fit kMaxAutoScratchBytes), at least 1
+//             least kMinShipRoundsPerCta rounds (SHIP) or kMinStepsPerCta
+//             unrolled steps (DIRECT) of keys, clusters whose partial rows
+//             fit kMaxAutoScratchBytes), at least 1
 #include <stdint.h>
 
 #include "internal.h"
@@ -174,8 +175,10 @@ int plan_shape(const dsmem_hist_device_t* dev, int32_t num_bins, int64_t n,
     }
     C = req->num_clusters;
   } else {
-    const int64_t keys_per_cluster = static_cast<int64_t>(P) * threads * kKeysPerThreadStep *
-                                     kMinStepsPerCta;
+    const int64_t keys_per_cluster =
+        kernel == DSMEM_HIST_KERNEL_SHIP
+            ? static_cast<int64_t>(P) * threads * kpt * kMinShipRoundsPerCta
+            : static_cast<int64_t>(P) * threads * kKeysPerThreadStep * kMinStepsPerCta;
     const int64_t need = ceil_div(n > 0 ? n : 1, keys_per_cluster);
     C = need < mac ? need : mac;
     // Bound the partial rows' scratch for very large bin counts.
