@@ -185,24 +185,42 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_traffic(n_keys, num_bins, cluster_size, kernel_id):
+# Files whose bytes decide the compiled cluster kernels: a change to any of
+# them invalidates the committed DRAM counters.
+KERNEL_DEPENDENCIES = [
+    os.path.join(ROOT, "cluster_distributed_shared_gb300", "csrc", "ptx.cuh"),
+    os.path.join(ROOT, "cluster_distributed_shared_gb300", "csrc", "internal.h"),
+    os.path.join(ROOT, "include", "dsmem_hist.h"),
+]
+
+
+def kernel_sources_sha256(kernel_id):
+    """sha256 over the kernel's source file and the headers it includes."""
+    h = hashlib.sha256()
+    for path in [KERNEL_SOURCES[kernel_id][1]] + KERNEL_DEPENDENCIES:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def kernel_traffic(n_keys, num_bins, cluster_size, kernel_id, block_threads):
     """Per-launch DRAM bytes of the cluster kernel from the committed ncu
-    summary, scaled to this launch's keys; None when the kernel source has
-    changed since the counters were taken."""
+    summary, scaled to this launch's keys; None when the kernel's sources or
+    its block size have changed since the counters were taken."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
-        name, source = KERNEL_SOURCES[kernel_id]
-        with open(source, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
+        name = KERNEL_SOURCES[kernel_id][0]
+        sha = kernel_sources_sha256(kernel_id)
         if not rec.get("kernel", "").startswith(name):
             return None
     except (OSError, ValueError, KeyError):
         return None
-    if rec.get("kernel_source_sha256") != sha:
+    if rec.get("kernel_sources_sha256") != sha:
         return None
     for e in rec.get("captures", []):
-        if e.get("num_bins") == num_bins and e.get("cluster_size") == cluster_size:
+        if (e.get("num_bins") == num_bins and e.get("cluster_size") == cluster_size
+                and e.get("block_threads") == block_threads):
             return e["dram_bytes"] * (n_keys / e["n"])
     return None
 
@@ -427,7 +445,7 @@ def run_ours(a, world, rank, local):
     peak, peak_src = hbm_peak()
     alg_bytes = 4 * n + 4 * num_bins
     achieved = alg_bytes / (cluster_ms / 1e3) / 1e9
-    traffic = kernel_traffic(n, num_bins, P, plan["kernel"])
+    traffic = kernel_traffic(n, num_bins, P, plan["kernel"], plan["block_threads"])
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",

@@ -28,7 +28,7 @@ DSMEM_HIST_ENOMEM = -5
 
 KERNEL_DIRECT = 0
 KERNEL_SHIP = 1
-SHIP_THREADS = 768  # DSMEM_HIST_SHIP_THREADS
+SHIP_THREADS = 896  # DSMEM_HIST_SHIP_THREADS
 
 
 class DsmemHistError(RuntimeError):

@@ -19,7 +19,7 @@
 //             per thread per round if that fits, else 4, with staging rows
 //             holding twice the expected entries per column (at least 1.5
 //             times); else DIRECT
-//   threads = kShipThreads (768) for SHIP; for DIRECT 1024 when only one CTA fits an SM,
+//   threads = kShipThreads (896) for SHIP; for DIRECT 1024 when only one CTA fits an SM,
 //             else 512
 //   C       = min(resident clusters, clusters needed so each CTA gets at
 //             least kMinShipRoundsPerCta rounds (SHIP) or kMinStepsPerCta

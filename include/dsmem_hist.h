@@ -64,7 +64,7 @@ enum {
 enum { DSMEM_HIST_KERNEL_DIRECT = 0, DSMEM_HIST_KERNEL_SHIP = 1 };
 
 /* Threads per CTA of the ship kernel (fixed at build time). */
-#define DSMEM_HIST_SHIP_THREADS 768
+#define DSMEM_HIST_SHIP_THREADS 896
 
 /* Launch shape chosen by the planner (all fields filled by dsmem_hist_plan*). */
 typedef struct dsmem_hist_plan {

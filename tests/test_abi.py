@@ -159,11 +159,11 @@ def test_planner_grid_and_threads():
     assert direct["block_threads"] == 512 and direct["kernel"] == pkg.KERNEL_DIRECT
     one = plan(GB300, 8192, 1 << 20, cluster_size=1)
     assert one["kernel"] == pkg.KERNEL_DIRECT      # no remote owners: local increments
-    # Ship kernel: about two rounds (768 threads x 8 keys) per CTA; direct
+    # Ship kernel: about two rounds (896 threads x 8 keys) per CTA; direct
     # kernel: four unrolled steps (16 keys per thread) per CTA.
     ship = plan(GB300, 8192, 1 << 20, mac=76)
     assert ship["kernel"] == pkg.KERNEL_SHIP and ship["keys_per_thread"] == 8
-    assert ship["num_clusters"] == -(-(1 << 20) // (2 * pkg.SHIP_THREADS * 8 * 2)) == 43
+    assert ship["num_clusters"] == -(-(1 << 20) // (2 * pkg.SHIP_THREADS * 8 * 2)) == 37
     assert plan(GB300, 8192, 1 << 30, mac=76)["num_clusters"] == 76
     d = plan(GB300, 8192, 1 << 20, mac=76, kernel=pkg.KERNEL_DIRECT)
     assert d["num_clusters"] == -(-(1 << 20) // (2 * d["block_threads"] * 16 * 4))
