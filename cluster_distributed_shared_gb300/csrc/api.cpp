@@ -53,6 +53,8 @@ struct DeviceState {
   int prepared_ship[2] = {0, 0};
   // (kernel, variant, P, threads, smem) -> resident clusters
   std::map<std::tuple<int, int, int, int, int>, int> occupancy;
+  // (kernel, variant, threads, smem) -> largest co-schedulable cluster size
+  std::map<std::tuple<int, int, int, int>, int> potential;
   std::mutex host_call;  // serialises dsmem_hist_host on this device
 };
 
@@ -168,6 +170,29 @@ int plan_locked(DeviceState* st, int32_t num_bins, int64_t n, const dsmem_hist_r
     if ((rc = prepare_locked(st, *out))) return rc;
     const bool ship = out->kernel == DSMEM_HIST_KERNEL_SHIP;
     const int variant = ship ? out->keys_per_thread : out->aggregate;
+    if (req.cluster_size == 0) {
+      // An automatic cluster size stays within the largest cluster this shape
+      // can be co-scheduled with (cudaOccupancyMaxPotentialClusterSize).
+      auto pkey = std::make_tuple(out->kernel, variant, out->block_threads, out->smem_bytes);
+      auto pit = st->potential.find(pkey);
+      int pcs = 0;
+      if (pit != st->potential.end()) {
+        pcs = pit->second;
+      } else {
+        e = ship ? query_ship_potential_cluster_size(out->keys_per_thread, out->smem_bytes, &pcs)
+                 : query_max_potential_cluster_size(out->aggregate, out->block_threads,
+                                                    out->smem_bytes, &pcs);
+        if (e != cudaSuccess) {
+          cudaGetLastError();
+          pcs = 0;
+        }
+        st->potential[pkey] = pcs;
+      }
+      if (pcs >= 1 && pcs < out->cluster_size && pcs < dev.max_cluster_size) {
+        dev.max_cluster_size = pcs;
+        continue;
+      }
+    }
     auto key = std::make_tuple(out->kernel, variant, out->cluster_size, out->block_threads,
                                out->smem_bytes);
     auto it = st->occupancy.find(key);

@@ -306,6 +306,17 @@ cudaError_t query_max_active_clusters(int aggregate, int cluster_size, int block
   return cudaOccupancyMaxActiveClusters(out, cluster_kernel(aggregate), &cfg);
 }
 
+// Largest cluster that can be co-scheduled for the direct kernel with this
+// block size and dynamic shared memory (non-portable sizes allowed).
+cudaError_t query_max_potential_cluster_size(int aggregate, int block_threads, int smem_bytes,
+                                             int* out) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(16, 1, 1);
+  cfg.blockDim = dim3(block_threads, 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes;
+  return cudaOccupancyMaxPotentialClusterSize(out, cluster_kernel(aggregate), &cfg);
+}
+
 cudaError_t launch_cluster_hist(const dsmem_hist_plan_t& plan, const ClusterHistArgs& args,
                                 cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};

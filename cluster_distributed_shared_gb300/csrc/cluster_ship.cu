@@ -473,6 +473,16 @@ cudaError_t query_ship_active_clusters(int kpt, int cluster_size, int smem_bytes
   return cudaOccupancyMaxActiveClusters(out, ship_kernel_ptr(kpt, true), &cfg);
 }
 
+// Largest cluster that can be co-scheduled for this kernel with `smem_bytes`
+// of dynamic shared memory per CTA (non-portable sizes allowed).
+cudaError_t query_ship_potential_cluster_size(int kpt, int smem_bytes, int* out) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(16, 1, 1);
+  cfg.blockDim = dim3(kShipThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes;
+  return cudaOccupancyMaxPotentialClusterSize(out, ship_kernel_ptr(kpt, true), &cfg);
+}
+
 cudaError_t launch_cluster_ship(const dsmem_hist_plan_t& plan, const ClusterHistArgs& args,
                                 cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};

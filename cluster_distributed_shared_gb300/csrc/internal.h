@@ -74,6 +74,11 @@ cudaError_t prepare_cluster_kernel(int aggregate, int smem_bytes);
 // Occupancy query: clusters of this shape that can be resident at once.
 cudaError_t query_max_active_clusters(int aggregate, int cluster_size, int block_threads,
                                       int smem_bytes, int* out);
+// Largest co-schedulable cluster size (cudaOccupancyMaxPotentialClusterSize)
+// for the direct and the ship kernel at a given shape.
+cudaError_t query_max_potential_cluster_size(int aggregate, int block_threads, int smem_bytes,
+                                             int* out);
+cudaError_t query_ship_potential_cluster_size(int keys_per_thread, int smem_bytes, int* out);
 
 // The whole histogram with partial rows in caller-supplied device memory of
 // at most max_rows_bytes (api.cpp; used by static_scratch.cu).

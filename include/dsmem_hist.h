@@ -244,8 +244,11 @@ enum {
 DSMEM_HIST_API int dsmem_hist_microbench(int32_t kind, int32_t cluster_size, int32_t iters,
                                          double* value, double* ms);
 
-/* Plan for the current device (queries its properties and the occupancy of
- * the chosen shape).  `request` may be NULL.
+/* Plan for the current device (queries its properties, the largest cluster
+ * the chosen kernel and shared-memory size can be co-scheduled with
+ * (cudaOccupancyMaxPotentialClusterSize, which caps an automatic cluster
+ * size), and the resident clusters of the chosen shape
+ * (cudaOccupancyMaxActiveClusters)).  `request` may be NULL.
  *
  * Every entry point that plans on the current device (dsmem_hist,
  * dsmem_hist_ex, dsmem_hist_host, dsmem_hist_static, dsmem_hist_plan) reads
