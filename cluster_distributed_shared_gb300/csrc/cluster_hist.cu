@@ -168,43 +168,71 @@ __global__ void __launch_bounds__(1024, 1) cluster_hist_kernel(const ClusterHist
   }
 }
 
-// bins[i] = sum over clusters c of partials[c][i] (mod 2^32).
+// bins[i] = sum over clusters c of partials[c][i] (mod 2^32).  A CTA owns
+// 256 / G columns of 16-byte vectors; its G row groups each sum every G-th
+// partial row of those columns with four loads in flight, so a thread waits
+// on about ceil(C / 4G) loads in turn instead of ceil(C / 4), and the groups'
+// sums meet in shared memory.
+template <int G>
 __global__ void __launch_bounds__(256) reduce_partials_kernel(const uint32_t* __restrict__ partials,
                                                               uint64_t stride, uint32_t num_clusters,
                                                               uint32_t num_bins,
                                                               uint32_t* __restrict__ bins,
                                                               int bins_vec_ok) {
+  constexpr uint32_t kCols = 256 / G;
+  __shared__ uint4 part[G][kCols];
+  const uint32_t col = threadIdx.x % kCols, g = threadIdx.x / kCols;
   const uint32_t nv = (num_bins + 3) / 4;
-  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += gridDim.x * blockDim.x) {
+  const size_t row4 = stride / 4;
+  for (uint32_t tile = blockIdx.x * kCols; tile < nv; tile += gridDim.x * kCols) {
+    const uint32_t i = tile + col;
     uint4 s = make_uint4(0, 0, 0, 0);
-    const uint4* p = reinterpret_cast<const uint4*>(partials) + i;
-    const size_t row4 = stride / 4;
-    uint32_t c = 0;
-    for (; c + 4 <= num_clusters; c += 4) {
-      const uint4 a0 = __ldcs(p + (c + 0) * row4);
-      const uint4 a1 = __ldcs(p + (c + 1) * row4);
-      const uint4 a2 = __ldcs(p + (c + 2) * row4);
-      const uint4 a3 = __ldcs(p + (c + 3) * row4);
-      s.x += a0.x + a1.x + a2.x + a3.x;
-      s.y += a0.y + a1.y + a2.y + a3.y;
-      s.z += a0.z + a1.z + a2.z + a3.z;
-      s.w += a0.w + a1.w + a2.w + a3.w;
+    if (i < nv) {
+      const uint4* p = reinterpret_cast<const uint4*>(partials) + i;
+      uint32_t c = g;
+      for (; c + 3 * G < num_clusters; c += 4 * G) {
+        const uint4 a0 = __ldcs(p + (c + 0 * G) * row4);
+        const uint4 a1 = __ldcs(p + (c + 1 * G) * row4);
+        const uint4 a2 = __ldcs(p + (c + 2 * G) * row4);
+        const uint4 a3 = __ldcs(p + (c + 3 * G) * row4);
+        s.x += a0.x + a1.x + a2.x + a3.x;
+        s.y += a0.y + a1.y + a2.y + a3.y;
+        s.z += a0.z + a1.z + a2.z + a3.z;
+        s.w += a0.w + a1.w + a2.w + a3.w;
+      }
+      for (; c < num_clusters; c += G) {
+        const uint4 a0 = __ldcs(p + c * row4);
+        s.x += a0.x;
+        s.y += a0.y;
+        s.z += a0.z;
+        s.w += a0.w;
+      }
     }
-    for (; c < num_clusters; ++c) {
-      const uint4 a0 = __ldcs(p + c * row4);
-      s.x += a0.x;
-      s.y += a0.y;
-      s.z += a0.z;
-      s.w += a0.w;
+    if (G > 1) {
+      part[g][col] = s;
+      __syncthreads();
+      if (g == 0) {
+#pragma unroll
+        for (int h = 1; h < G; ++h) {
+          const uint4 o = part[h][col];
+          s.x += o.x;
+          s.y += o.y;
+          s.z += o.z;
+          s.w += o.w;
+        }
+      }
+      __syncthreads();  // part is rewritten by the next tile
     }
-    const uint32_t b = 4 * i;
-    if (bins_vec_ok && b + 3 < num_bins) {
-      reinterpret_cast<uint4*>(bins)[i] = s;
-    } else {
-      if (b + 0 < num_bins) bins[b + 0] = s.x;
-      if (b + 1 < num_bins) bins[b + 1] = s.y;
-      if (b + 2 < num_bins) bins[b + 2] = s.z;
-      if (b + 3 < num_bins) bins[b + 3] = s.w;
+    if (g == 0 && i < nv) {
+      const uint32_t b = 4 * i;
+      if (bins_vec_ok && b + 3 < num_bins) {
+        reinterpret_cast<uint4*>(bins)[i] = s;
+      } else {
+        if (b + 0 < num_bins) bins[b + 0] = s.x;
+        if (b + 1 < num_bins) bins[b + 1] = s.y;
+        if (b + 2 < num_bins) bins[b + 2] = s.z;
+        if (b + 3 < num_bins) bins[b + 3] = s.w;
+      }
     }
   }
 }
@@ -339,11 +367,28 @@ cudaError_t launch_reduce_partials(const uint32_t* partials, uint64_t stride,
                                    uint32_t num_clusters, uint32_t num_bins, uint32_t* bins,
                                    cudaStream_t stream) {
   const uint32_t nv = (num_bins + 3) / 4;
-  uint32_t blocks = (nv + 255) / 256;
-  if (blocks > 4096) blocks = 4096;
   const int vec_ok = (reinterpret_cast<uintptr_t>(bins) & 15u) == 0;
-  reduce_partials_kernel<<<blocks, 256, 0, stream>>>(partials, stride, num_clusters, num_bins,
-                                                     bins, vec_ok);
+  // Row groups: the largest power of two <= min(16, C).
+  int G = 1;
+  while (G < 16 && static_cast<uint32_t>(2 * G) <= num_clusters) G *= 2;
+  uint32_t blocks = (nv + (256 / G) - 1) / (256 / G);
+  if (blocks > 8192) blocks = 8192;
+  switch (G) {
+    case 16:
+      reduce_partials_kernel<16><<<blocks, 256, 0, stream>>>(partials, stride, num_clusters, num_bins, bins, vec_ok);
+      break;
+    case 8:
+      reduce_partials_kernel<8><<<blocks, 256, 0, stream>>>(partials, stride, num_clusters, num_bins, bins, vec_ok);
+      break;
+    case 4:
+      reduce_partials_kernel<4><<<blocks, 256, 0, stream>>>(partials, stride, num_clusters, num_bins, bins, vec_ok);
+      break;
+    case 2:
+      reduce_partials_kernel<2><<<blocks, 256, 0, stream>>>(partials, stride, num_clusters, num_bins, bins, vec_ok);
+      break;
+    default:
+      reduce_partials_kernel<1><<<blocks, 256, 0, stream>>>(partials, stride, num_clusters, num_bins, bins, vec_ok);
+  }
   return cudaGetLastError();
 }
 
