@@ -348,6 +348,8 @@ int run_partials(const int32_t* keys, int64_t n, int32_t num_bins, const dsmem_h
     DeviceState* st = nullptr;
     if ((rc = device_state(&st))) return rc;
     if ((rc = check_plan(st, plan, num_bins))) return rc;
+    if (plan->kernel == DSMEM_HIST_KERNEL_SHIP && n >= kShipMaxKeys)
+      return fail(DSMEM_HIST_EINVAL, "the ship kernel takes fewer than 2^38 keys per call");
     if ((rc = prepare_locked(st, *plan))) return rc;
   }
   const ClusterHistArgs args = make_args(*plan, keys, n, num_bins, partials, accumulate);

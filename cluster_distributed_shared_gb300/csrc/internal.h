@@ -25,6 +25,9 @@ constexpr int kMinShipRoundsPerCta = 2;
 constexpr int kDefaultSliceCapBytes = 128 * 1024;
 // Scratch bound the planner keeps the partial rows under when it picks C.
 constexpr int64_t kMaxAutoScratchBytes = int64_t{1} << 30;
+// The ship kernel indexes 512-byte warp tiles with 32-bit integers (and adds
+// up to three rounds of tiles to them): it takes fewer keys than this.
+constexpr int64_t kShipMaxKeys = int64_t{1} << 38;
 // Threads per CTA of the ship kernel.
 constexpr int kShipThreads = DSMEM_HIST_SHIP_THREADS;
 // Shared memory the runtime reserves per CTA on sm_90 and later.

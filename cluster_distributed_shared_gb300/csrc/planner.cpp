@@ -113,7 +113,12 @@ int plan_shape(const dsmem_hist_device_t* dev, int32_t num_bins, int64_t n,
   // staging fits beside the slice (kShipThreads threads), else direct increments.
   int kernel = DSMEM_HIST_KERNEL_DIRECT, kpt = 0, nq = 0;
   const bool ship_ok_threads = req->block_threads == 0 || req->block_threads == kShipThreads;
-  if (req->kernel == DSMEM_HIST_KERNEL_SHIP || (req->kernel < 0 && P >= 2 && ship_ok_threads)) {
+  if (req->kernel == DSMEM_HIST_KERNEL_SHIP ||
+      (req->kernel < 0 && P >= 2 && ship_ok_threads && n < kShipMaxKeys)) {
+    if (n >= kShipMaxKeys) {
+      *why = "the ship kernel takes fewer than 2^38 keys per call";
+      return DSMEM_HIST_EINVAL;
+    }
     if (P < 2 || !ship_ok_threads) {
       if (req->kernel == DSMEM_HIST_KERNEL_SHIP) {
         *why = "the ship kernel needs cluster_size >= 2 and its fixed block size";

@@ -171,6 +171,17 @@ def test_planner_grid_and_threads():
     assert forced["num_clusters"] == 7 and forced["block_threads"] == 256
 
 
+def test_planner_keeps_huge_inputs_off_the_ship_kernel():
+    # The ship kernel indexes warp tiles with 32-bit integers: from 2^38 keys
+    # on the planner picks the direct kernel, and refuses a forced ship kernel.
+    assert plan(GB300, 262144, (1 << 38) - 1, mac=15)["kernel"] == pkg.KERNEL_SHIP
+    big = plan(GB300, 262144, 1 << 38, mac=15)
+    assert big["kernel"] == pkg.KERNEL_DIRECT and big["cluster_size"] == 8
+    with pytest.raises(pkg.DsmemHistError) as e:
+        plan(GB300, 262144, 1 << 38, mac=15, kernel=pkg.KERNEL_SHIP)
+    assert e.value.code == pkg.DSMEM_HIST_EINVAL
+
+
 def test_planner_multi_pass_when_bins_exceed_cluster():
     p = plan(GB300, 1 << 22, 1 << 24)
     assert p["cluster_size"] == 16 and p["passes"] == 8 and p["bins_per_cta"] == 32768
