@@ -35,12 +35,8 @@ __device__ __forceinline__ void cluster_barrier() {
       "barrier.cluster.arrive.release.aligned;\n\t"
       "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// The two halves, for overlapping the barrier's latency with local work.
-__device__ __forceinline__ void cluster_arrive() {
-  __syncwarp();
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-// Arrival without release ordering: for threads that published no remote
+// The barrier in two halves, for overlapping its latency with local work.
+// The arrival has no release ordering: for threads that published no remote
 // writes since the last phase.
 __device__ __forceinline__ void cluster_arrive_relaxed() {
   __syncwarp();
@@ -49,12 +45,6 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
 __device__ __forceinline__ void cluster_wait() {
   __syncwarp();
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Barrier among `count` threads (a multiple of 32) of this CTA on hardware
-// barrier `id` (0 is the one __syncthreads uses).
-__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // mbarrier helpers (shared::cta addresses unless noted).
@@ -124,11 +114,6 @@ __device__ __forceinline__ uint32_t atom_add_local(uint32_t cta_addr, uint32_t v
   asm volatile("atom.shared.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(cta_addr), "r"(v));
   return old;
 }
-__device__ __forceinline__ uint16_t ld_shared_u16(uint32_t cta_addr) {
-  uint16_t v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(cta_addr));
-  return v;
-}
 
 // Asm statements without a "memory" clobber are still volatile, so they keep
 // their order relative to each other and to the barriers above (which do
@@ -137,9 +122,6 @@ __device__ __forceinline__ uint16_t ld_shared_u16(uint32_t cta_addr) {
 __device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, const uint4& v) {
   asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(v.x),
                "r"(v.y), "r"(v.z), "r"(v.w));
-}
-__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v));
 }
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t cta_addr) {
   uint4 v;
@@ -159,9 +141,6 @@ __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t cta_addr) {
   uint32_t v;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(cta_addr));
   return v;
-}
-__device__ __forceinline__ void st_shared_u16(uint32_t cta_addr, uint16_t v) {
-  asm volatile("st.shared.u16 [%0], %1;" ::"r"(cta_addr), "h"(v));
 }
 // Release stores and acquire loads for flag passing between CTAs.
 __device__ __forceinline__ void st_release_cluster(uint32_t cluster_addr, uint32_t v) {
