@@ -243,7 +243,8 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
   const uint32_t inbox0 = stage0 + 2u * buf_bytes;
 
   // Key stream: warp tiles of 32 vectors (tile t = vectors 32t .. 32t+31),
-  // kKpt/4 tiles per warp per round; tile indices fit 32 bits (n < 2^39).
+  // kKpt/4 tiles per warp per round; tile indices fit 32 bits with room for
+  // three rounds on top (the library keeps n below 2^38 for this kernel).
   constexpr uint32_t kWarps = kShipThreads / 32;
   const uint32_t nwarps = gridDim.x * kWarps;
   const uint32_t gwarp = blockIdx.x * kWarps + warp;
