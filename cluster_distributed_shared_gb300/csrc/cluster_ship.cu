@@ -103,10 +103,11 @@ __device__ __forceinline__ void stage_entry(uint32_t ea, uint32_t lim, uint32_t 
 
 // Partition one warp tile (four keys per lane).  All four reservations are
 // issued before the first store so their latencies overlap.  kBase0: the
-// pass starts at bin 0, so a key is its own in-pass offset.
-template <bool kPow2, bool kBase0>
+// pass starts at bin 0, so a key is its own in-pass offset.  kRunTest: test
+// first whether the tile holds one key (off when the caller already has).
+template <bool kPow2, bool kBase0, bool kRunTest>
 __device__ __forceinline__ void partition_tile(const int4& v, const Ctx& c) {
-  if (__all_sync(kFullMask, v.x == v.w)) {  // rare on most inputs: then test the whole tile
+  if (kRunTest && __all_sync(kFullMask, v.x == v.w)) {  // rare on most inputs: then test the whole tile
     const int32_t k0 = __shfl_sync(kFullMask, v.x, 0);
     const bool eq4 = (v.x == v.y) & (v.y == v.z) & (v.z == v.w);
     if (__all_sync(kFullMask, eq4 & (v.x == k0))) {
@@ -144,12 +145,40 @@ __device__ __forceinline__ void partition_tile(const int4& v, const Ctx& c) {
 
 template <int kTiles, bool kPow2>
 __device__ __forceinline__ void partition_round(const int4 (&v)[kTiles], const Ctx& c) {
+  static_assert(kTiles == 1 || kTiles == 2, "one or two tiles per warp and round");
+  // The warp's tiles are consecutive in the input.  The first tile's run test
+  // runs here: a run tile followed by a run tile of the same key (a run of
+  // 256) becomes one remote red, a lone run tile one red of 128.
+  if (__all_sync(kFullMask, v[0].x == v[0].w)) {  // rare on most inputs
+    const int32_t k0 = __shfl_sync(kFullMask, v[0].x, 0);
+    const bool eq0 = (v[0].x == v[0].y) & (v[0].y == v[0].z) & (v[0].z == v[0].w) & (v[0].x == k0);
+    if (__all_sync(kFullMask, eq0)) {
+      const int4& w = v[kTiles - 1];
+      const bool eq1 = (w.x == k0) & (w.y == k0) & (w.z == k0) & (w.w == k0);
+      const bool both = kTiles == 2 && __all_sync(kFullMask, eq1);
+      const uint32_t rel = static_cast<uint32_t>(k0) - c.base;
+      if (c.lane == 0 && rel < c.range) {
+        uint32_t o, loc;
+        owner_local(rel, c, o, loc, kPow2);
+        red_add_cluster(map_rank(c.slice + 4u * loc, o), both ? 256u : 128u);
+      }
+      if (kTiles == 1 || both) return;
+      if (c.base == 0)
+        partition_tile<kPow2, true, true>(w, c);
+      else
+        partition_tile<kPow2, false, true>(w, c);
+      return;
+    }
+  }
+  // Past here the first tile is known not to be a run.
   if (c.base == 0) {
+    partition_tile<kPow2, true, false>(v[0], c);
 #pragma unroll
-    for (int u = 0; u < kTiles; ++u) partition_tile<kPow2, true>(v[u], c);
+    for (int u = 1; u < kTiles; ++u) partition_tile<kPow2, true, true>(v[u], c);
   } else {
+    partition_tile<kPow2, false, false>(v[0], c);
 #pragma unroll
-    for (int u = 0; u < kTiles; ++u) partition_tile<kPow2, false>(v[u], c);
+    for (int u = 1; u < kTiles; ++u) partition_tile<kPow2, false, true>(v[u], c);
   }
 }
 
@@ -188,19 +217,20 @@ __device__ __forceinline__ uint4 pad_vector(uint32_t pad0) {
   return make_uint4(pad0, pad0 + 0x00020002u, pad0 + 0x00040004u, pad0 + 0x00060006u);
 }
 
-// Loads a round's tiles t0 + u * nwarps; tiles past the end read as keys -1
-// (outside every pass).  Only the last round can reach past the end.
+// Loads a warp's consecutive tiles t0, t0 + 1, ... of a round; tiles past
+// the end read as keys -1 (outside every pass).  Only the last round can
+// reach past the end.
 template <int kKpt>
 __device__ __forceinline__ void load_round(int4 (&v)[kKpt / 4], const int4* vec, uint32_t ntiles,
-                                           uint32_t t0, uint32_t nwarps, bool last) {
+                                           uint32_t t0, bool last) {
   if (!last) {
 #pragma unroll
-    for (int u = 0; u < kKpt / 4; ++u) v[u] = ld_stream_v4(vec + static_cast<size_t>(t0 + u * nwarps) * 32u);
+    for (int u = 0; u < kKpt / 4; ++u) v[u] = ld_stream_v4(vec + static_cast<size_t>(t0 + u) * 32u);
     return;
   }
 #pragma unroll
   for (int u = 0; u < kKpt / 4; ++u) {
-    const uint32_t t = t0 + u * nwarps;
+    const uint32_t t = t0 + u;
     v[u] = t < ntiles ? ld_stream_v4(vec + static_cast<size_t>(t) * 32u) : make_int4(-1, -1, -1, -1);
   }
 }
@@ -243,7 +273,7 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
   const uint32_t inbox0 = stage0 + 2u * buf_bytes;
 
   // Key stream: warp tiles of 32 vectors (tile t = vectors 32t .. 32t+31),
-  // kKpt/4 tiles per warp per round; tile indices fit 32 bits with room for
+  // kKpt/4 consecutive tiles per warp per round; tile indices fit 32 bits with room for
   // three rounds on top (the library keeps n below 2^38 for this kernel).
   constexpr uint32_t kWarps = kShipThreads / 32;
   const uint32_t nwarps = gridDim.x * kWarps;
@@ -252,6 +282,7 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
   const int4* vec = reinterpret_cast<const int4*>(a.keys + a.head) + c.lane;
   constexpr int kTiles = kKpt / 4;
   const uint32_t per_round = nwarps * kTiles;
+  const uint32_t wtile0 = gwarp * kTiles;  // this warp's first tile of round 0
   const uint32_t rounds = static_cast<uint32_t>((static_cast<uint64_t>(ntiles) + per_round - 1) / per_round);
 
   // Ship and apply: warp w serves owner (and sender) w mod P, as member sg of
@@ -308,11 +339,11 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
 
     int4 cur[kTiles];
     if (rounds > 0) {
-      load_round<kKpt>(cur, vec, ntiles, gwarp, nwarps, rounds == 1);
+      load_round<kKpt>(cur, vec, ntiles, wtile0, rounds == 1);
       c.cur_lane = cur_lane0;
       c.lim0 = stage0 + c.blk;
       partition_round<kTiles, kPow2>(cur, c);
-      if (rounds > 1) load_round<kKpt>(cur, vec, ntiles, gwarp + per_round, nwarps, rounds == 2);
+      if (rounds > 1) load_round<kKpt>(cur, vec, ntiles, wtile0 + per_round, rounds == 2);
     }
     __syncthreads();  // round 0 staged
     uint32_t k = 0;  // r % 3
@@ -369,7 +400,7 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
         c.lim0 = stage0 + (b ^ 1u) * buf_bytes + c.blk;
         partition_round<kTiles, kPow2>(cur, c);
         if (r + 2 < rounds)
-          load_round<kKpt>(cur, vec, ntiles, gwarp + (r + 2) * per_round, nwarps, r + 3 == rounds);
+          load_round<kKpt>(cur, vec, ntiles, wtile0 + (r + 2) * per_round, r + 3 == rounds);
       }
       cluster_wait();   // round r's inboxes complete everywhere
       __syncthreads();  // round r + 1 staged; round r's staging and cursors read
