@@ -66,6 +66,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--keys", type=int, default=0,
+                    help="scale the workload to this many keys, same distribution (profiling of "
+                         "smaller cases; default: the workload's own length)")
     ap.add_argument("--cluster", type=int, default=0,
                     help="cluster size (default: the workload's published one)")
     a = ap.parse_args()
@@ -73,6 +76,8 @@ def parse():
         ap.error("--warmup must be >= 3")
     if a.steps < 1:
         ap.error("--steps must be >= 1")
+    if a.keys < 0 or (a.keys and a.keys % 512):
+        ap.error("--keys must be a positive multiple of 512 (whole runs of 256 in either half)")
     return a
 
 
@@ -83,9 +88,13 @@ def dist_env():
     return world, rank, local
 
 
-def workload_config(name, seed):
+def workload_config(name, seed, keys=0):
+    """The named workload's description; `keys` > 0 scales it to that many keys
+    (same distribution; a profiling aid, reported in the config)."""
     import gen
-    w = gen.WORKLOADS[name]
+    w = dict(gen.WORKLOADS[name])
+    if keys:
+        w["n"] = keys
     return {
         "workload": name,
         "n": w["n"],
@@ -95,6 +104,7 @@ def workload_config(name, seed):
         "cluster_size": WORKLOAD_CLUSTER[name],
         "l2": "inputs larger than L2 (no flush)" if 4 * w["n"] > L2_BYTES
         else "inputs L2-resident (smaller than L2; no flush)",
+        **({"keys_override": True} if keys else {}),
     }
 
 
@@ -279,8 +289,8 @@ def run_reference(a, world, rank):
         return
     import gen
     import oracle
-    cfg = workload_config(a.workload, a.seed)
-    keys = gen.workload(a.workload, a.seed)
+    cfg = workload_config(a.workload, a.seed, a.keys)
+    keys = gen.workload(a.workload, a.seed, n=cfg["n"])
     n, num_bins = cfg["n"], cfg["num_bins"]
     # Size each step's sample so the whole run stays around a minute.
     probe = keys[: 1 << 20]
@@ -332,12 +342,12 @@ def run_ours(a, world, rank, local):
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
 
-    cfg = workload_config(a.workload, a.seed)
+    cfg = workload_config(a.workload, a.seed, a.keys)
     seed = replica_seed(a.seed, rank)
     if a.cluster:
         cfg["cluster_size"] = a.cluster
     n, num_bins, P = cfg["n"], cfg["num_bins"], cfg["cluster_size"]
-    keys_h = gen.workload(a.workload, seed)
+    keys_h = gen.workload(a.workload, seed, n=cfg["n"])
     keys = torch.from_numpy(keys_h).to(dev)
     plan = pkg.dsmem_hist_plan(num_bins, n, cluster_size=P)
     partials = torch.empty(plan["num_clusters"] * plan["partial_stride"], dtype=torch.int32,

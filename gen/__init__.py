@@ -143,13 +143,15 @@ def zipf_tables(num_bins: int, s: float, seed: int):
 
 
 def workload(name: str, seed: int, out: np.ndarray | None = None,
-             threads: int | None = None) -> np.ndarray:
-    """Keys of one named workload (see the module table) for this seed."""
+             threads: int | None = None, n: int | None = None) -> np.ndarray:
+    """Keys of one named workload (see the module table) for this seed; `n`
+    scales it to another length with the same distribution and layout."""
     w = WORKLOADS[name]
+    n = w["n"] if n is None else n
     if w["dist"] == "uniform":
-        return uniform(w["n"], w["num_bins"], seed, out, threads)
+        return uniform(n, w["num_bins"], seed, out, threads)
     if w["dist"] == "zipf":
-        return zipf(w["n"], w["num_bins"], seed, w["s"], out, threads)
+        return zipf(n, w["num_bins"], seed, w["s"], out, threads)
     if w["dist"] == "runs":
-        return runs(w["n"], w["num_bins"], seed, w["run_len"], out, threads)
+        return runs(n, w["num_bins"], seed, w["run_len"], out, threads)
     raise KeyError(name)

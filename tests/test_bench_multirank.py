@@ -51,7 +51,7 @@ def test_whole_job_rate_counts_every_rank():
 
 def test_reference_arm_runs_on_rank_zero_only():
     class A:
-        workload, seed, steps, warmup = "uniform-1M-8K", 0, 5, 3
+        workload, seed, steps, warmup, keys = "uniform-1M-8K", 0, 5, 3, 0
     buf = io.StringIO()
     with redirect_stdout(buf):
         bench.run_reference(A, world=2, rank=1)
@@ -62,3 +62,17 @@ def test_reference_arm_runs_on_rank_zero_only():
     line = json.loads(buf.getvalue().strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_keys_override_scales_a_workload():
+    import numpy as np
+    import gen
+    cfg = bench.workload_config("runs256-1G-512K", 0, 1 << 20)
+    assert cfg["n"] == 1 << 20 and cfg["num_bins"] == 524288 and cfg["keys_override"]
+    assert "keys_override" not in bench.workload_config("runs256-1G-512K", 0)
+    k = gen.workload("runs256-1G-512K", 3, n=1 << 12)
+    assert k.size == 1 << 12
+    # Same layout as the full workload: uniform first half, runs of 256 after it.
+    runs = k[2048:].reshape(-1, 256)
+    assert (runs == runs[:, :1]).all() and runs.shape == (8, 256)
+    assert np.unique(k[:2048]).size > 1000
