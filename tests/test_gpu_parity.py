@@ -155,6 +155,53 @@ def test_ship_overflow_and_runs_paths():
             assert np.array_equal(got, want), (num_bins, P, kw)
 
 
+def test_ship_run_tiles_pairs_and_boundaries():
+    # The ship kernel deals each warp two consecutive 128-key tiles per round
+    # and turns a run tile followed by a run tile of the same key into one
+    # remote red of 256.  Built per 128-key tile: pairs of equal run tiles,
+    # run tiles with different keys side by side, runs that straddle a pair
+    # (odd-aligned runs of 256), runs of keys outside the bins, run tiles next
+    # to ordinary tiles; at several pointer offsets (the tiles then start
+    # mid-run) and in a multi-pass shape.
+    rng = np.random.default_rng(11)
+    ntiles = 1 << 14
+    kinds = rng.integers(0, 6, ntiles // 2)
+    tiles = []
+    for kind in kinds:
+        a, b = rng.integers(0, 262144, 2)
+        if kind == 0:     # one run of 256 on the pair
+            tiles += [np.full(128, a), np.full(128, a)]
+        elif kind == 1:   # two runs of 128, different keys
+            tiles += [np.full(128, a), np.full(128, b)]
+        elif kind == 2:   # run then ordinary tile
+            tiles += [np.full(128, a), rng.integers(0, 262144, 128)]
+        elif kind == 3:   # ordinary tile then run
+            tiles += [rng.integers(0, 262144, 128), np.full(128, a)]
+        elif kind == 4:   # runs of keys no bin holds (dropped), one negative
+            tiles += [np.full(128, 262144 + a), np.full(128, -1 - a)]
+        else:             # a run of 256 shifted by one tile: straddles two pairs
+            tiles += [np.full(128, b), np.full(128, a)]
+    keys = np.concatenate(tiles).astype(np.int32)
+    # kind 5 pairs end with key a; let the next pair start with the same key
+    # where it is also a run, so some runs of 256 start at an odd tile.
+    for t in range(1, ntiles - 1, 2):
+        if kinds[t // 2] == 5 and t + 1 < ntiles and rng.random() < 0.5:
+            keys[(t + 1) * 128:(t + 2) * 128] = keys[t * 128]
+    for off in (0, 1, 3):
+        k = keys[off:]
+        for num_bins, P in ((262144, 8), (524288, 16)):
+            want = oracle.histogram(k, num_bins)
+            got = gpu_hist(k, num_bins, cluster_size=P, kernel=SH)
+            assert np.array_equal(got, want), (off, num_bins, P)
+    # Eight passes of 32768 bins each: most runs hold keys of another pass.
+    want = oracle.histogram(keys, 262144)
+    plan = pkg.dsmem_hist_plan(262144, keys.size, cluster_size=2, kernel=SH,
+                               max_slice_bytes=4 * 16384)
+    assert plan["passes"] == 8 and plan["kernel"] == SH
+    got = gpu_hist(keys, 262144, cluster_size=2, kernel=SH, max_slice_bytes=4 * 16384)
+    assert np.array_equal(got, want)
+
+
 def test_ship_mostly_out_of_range_and_multi_pass():
     # Keys outside the pass meet the always-full cursor row and leave through
     # the spill path on almost every tile; later passes subtract their base.
