@@ -25,7 +25,8 @@
 //     full goes to its owner with a remote red (exact, slow, only on skewed
 //     rounds); a key outside the pass's bins meets a cursor row that is
 //     always full and is dropped on the same path.  A warp tile of 128 equal
-//     keys becomes one remote red of 128 (pre-aggregation of runs).
+//     keys becomes one remote red of 128, and a warp's two consecutive tiles
+//     of one key one red of 256 (pre-aggregation of runs).
 //   Ship.  Warps serve owner w mod P: the block's row count is the fullest
 //     column's fill, and its rows go out as contiguous 16-byte `st.async`
 //     stores into the owner's inbox slot for this sender, then are
