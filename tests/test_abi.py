@@ -43,6 +43,36 @@ def test_library_exports_every_declared_symbol():
     assert set(pkg.EXPORTS) <= set(names)
 
 
+def test_header_compiles_as_c_and_links(tmp_path):
+    # A C11 program (tests/c_abi_check.c) includes the header and calls the
+    # host-only entry points through libdsmemhist.so: the boundary is a C ABI.
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    from cluster_distributed_shared_gb300 import _build
+    lib = pkg.lib()._name
+    cuda_inc = None
+    for base in filter(None, [os.environ.get("CUDA_HOME"), os.path.dirname(os.path.dirname(_build.nvcc())),
+                              "/usr/local/cuda"]):
+        if os.path.exists(os.path.join(base, "include", "cuda_runtime_api.h")):
+            cuda_inc = os.path.join(base, "include")
+            break
+    if cuda_inc is None:
+        pytest.skip("cuda_runtime_api.h not found")
+    exe = str(tmp_path / "c_abi_check")
+    cmd = [gcc, "-std=c11", "-Wall", "-Wextra", "-Werror",
+           "-I", os.path.join(ROOT, "include"), "-I", cuda_inc,
+           os.path.join(ROOT, "tests", "c_abi_check.c"), lib,
+           "-Wl,-rpath," + os.path.dirname(lib), "-o", exe]
+    subprocess.run(cmd, check=True, capture_output=True, text=True)
+    out = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0, out.stdout + out.stderr
+    assert out.stdout.strip().endswith("ok")
+    assert f"block_threads={pkg.SHIP_THREADS}" in out.stdout
+
+
 def test_version_and_strerror():
     assert pkg.dsmem_hist_version() >= 100
     for code in (0, -1, -2, -3, -4, -5):
