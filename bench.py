@@ -298,8 +298,7 @@ def run_reference(a, world, rank):
     oracle.histogram(probe, num_bins)
     t_key = max((time.perf_counter() - t0) / probe.size, 1e-10)
     sample = int(min(n, max(1 << 16, 40.0 / ((a.steps + a.warmup) * t_key))))
-    sample -= sample % 4096 or 0
-    sample = max(sample, 4096)
+    sample = max(sample - sample % 4096, 4096)
     out = np.empty(num_bins, np.uint32)
     chunks = max(1, n // sample)
     for k in range(a.warmup):
