@@ -8,7 +8,7 @@ calls raise.
 
 Names follow the C ABI: ``dsmem_hist``, ``dsmem_hist_ex``,
 ``dsmem_hist_global_atomic``, ``dsmem_hist_host``, ``dsmem_hist_plan``,
-``dsmem_hist_plan_for_device``, ``dsmem_hist_release``.
+``dsmem_hist_plan_ex``, ``dsmem_hist_plan_for_device``, ``dsmem_hist_release``.
 """
 from __future__ import annotations
 
@@ -96,7 +96,7 @@ EXPORTS = (
     "dsmem_hist", "dsmem_hist_ex", "dsmem_hist_global_atomic", "dsmem_hist_host",
     "dsmem_hist_partials", "dsmem_hist_reduce", "dsmem_hist_static", "dsmem_hist_tune",
     "dsmem_hist_microbench",
-    "dsmem_hist_plan", "dsmem_hist_plan_for_device", "dsmem_hist_strerror",
+    "dsmem_hist_plan", "dsmem_hist_plan_ex", "dsmem_hist_plan_for_device", "dsmem_hist_strerror",
     "dsmem_hist_last_error", "dsmem_hist_release", "dsmem_hist_device_status",
     "dsmem_hist_version",
 )
@@ -130,7 +130,8 @@ def lib():
                 ("dsmem_hist_host", [p, i64, i32, p, p]),
                 ("dsmem_hist_partials", [p, i64, i32, ctypes.POINTER(Plan), p, i32, p]),
                 ("dsmem_hist_reduce", [p, i32, i64, i32, p, p]),
-                ("dsmem_hist_plan", [i32, i64, ctypes.POINTER(Request), ctypes.POINTER(Plan)]),
+                ("dsmem_hist_plan", [i32, i64, ctypes.POINTER(Plan)]),
+                ("dsmem_hist_plan_ex", [i32, i64, ctypes.POINTER(Request), ctypes.POINTER(Plan)]),
                 ("dsmem_hist_plan_for_device", [ctypes.POINTER(Device), i32, i64,
                                                 ctypes.POINTER(Request), i32,
                                                 ctypes.POINTER(Plan)]),
@@ -367,10 +368,23 @@ def dsmem_hist_tune(keys, num_bins: int, sample_keys: int = 0, stream=None) -> l
 
 
 def dsmem_hist_plan(num_bins: int, n: int, **overrides) -> dict:
-    """The launch shape the library would use on the current device."""
+    """The launch shape the library would use on the current device
+    (``dsmem_hist_plan``; with keyword overrides, ``dsmem_hist_plan_ex``)."""
     plan = Plan()
-    req = _request(**overrides)
-    _check(lib().dsmem_hist_plan(int(num_bins), int(n), ctypes.byref(req), ctypes.byref(plan)))
+    if overrides:
+        req = _request(**overrides)
+        _check(lib().dsmem_hist_plan_ex(int(num_bins), int(n), ctypes.byref(req),
+                                        ctypes.byref(plan)))
+    else:
+        _check(lib().dsmem_hist_plan(int(num_bins), int(n), ctypes.byref(plan)))
+    return plan.as_dict()
+
+
+def dsmem_hist_plan_ex(num_bins: int, n: int, request: Request) -> dict:
+    """dsmem_hist_plan with an explicit `Request` of planner overrides."""
+    plan = Plan()
+    _check(lib().dsmem_hist_plan_ex(int(num_bins), int(n), ctypes.byref(request),
+                                    ctypes.byref(plan)))
     return plan.as_dict()
 
 

@@ -674,14 +674,19 @@ int dsmem_hist_reduce(const uint32_t* partials, int32_t num_clusters, int64_t pa
   return run_reduce(partials, num_clusters, partial_stride, num_bins, bins, stream);
 }
 
-int dsmem_hist_plan(int32_t num_bins, int64_t n, const dsmem_hist_request_t* request,
-                    dsmem_hist_plan_t* out) {
+int dsmem_hist_plan_ex(int32_t num_bins, int64_t n, const dsmem_hist_request_t* request,
+                       dsmem_hist_plan_t* out) {
   if (!out) return fail(DSMEM_HIST_EINVAL, "out is NULL");
+  if (n < 0) return fail(DSMEM_HIST_EINVAL, "n must be >= 0 (got %lld)", static_cast<long long>(n));
   std::lock_guard<std::mutex> g(g_mutex);
   DeviceState* st = nullptr;
   int rc = device_state(&st);
   if (rc) return rc;
   return plan_locked(st, num_bins, n, request, out);
+}
+
+int dsmem_hist_plan(int32_t num_bins, int64_t n, dsmem_hist_plan_t* out) {
+  return dsmem_hist_plan_ex(num_bins, n, nullptr, out);
 }
 
 int dsmem_hist_plan_for_device(const dsmem_hist_device_t* device, int32_t num_bins, int64_t n,

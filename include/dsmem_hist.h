@@ -244,23 +244,54 @@ enum {
 DSMEM_HIST_API int dsmem_hist_microbench(int32_t kind, int32_t cluster_size, int32_t iters,
                                          double* value, double* ms);
 
-/* Plan for the current device (queries its properties, the largest cluster
- * the chosen kernel and shared-memory size can be co-scheduled with
- * (cudaOccupancyMaxPotentialClusterSize, which caps an automatic cluster
- * size), and the resident clusters of the chosen shape
- * (cudaOccupancyMaxActiveClusters)).  `request` may be NULL.
+/* The launch shape dsmem_hist would use on the current device for num_bins
+ * bins and n keys: cluster size P, counters per CTA S, passes, threads per
+ * CTA, clusters C, dynamic shared memory per CTA and the partial-row scratch.
+ *
+ * Where the rules come from:
+ *   - "Distributed Shared Memory", section "The cluster histogram": the bins
+ *     are split into P equal slices of S counters, one per CTA of a cluster,
+ *     and the page's kernel needs P * S to cover every bin (a smaller total
+ *     reaches past the cluster, a larger one drops bins).  Here S =
+ *     ceil(num_bins / (P * passes)) rounded up to a multiple of 4, so no bin
+ *     is dropped; the last CTA's few extra counters are never hit.
+ *   - CUDA Handbook, chapter 7, "Thread Block Clusters and Distributed Shared
+ *     Memory": up to 8 CTAs form a cluster portably and 16 as a non-portable
+ *     opt-in; the largest usable size for a kernel is what
+ *     cudaOccupancyMaxPotentialClusterSize reports; the shape is set at
+ *     launch through cudaLaunchKernelEx with a
+ *     cudaLaunchAttributeClusterDimension attribute.  The planner takes P
+ *     from 2..16 (16 after setting the non-portable attribute) and confirms
+ *     it, and the number of resident clusters, with
+ *     cudaOccupancyMaxPotentialClusterSize and cudaOccupancyMaxActiveClusters.
+ *   - "@dynshared", section "What it changes": static shared memory stops at
+ *     48 KB per CTA, and more comes only as dynamic shared memory requested at
+ *     launch.  A slice of 4*S bytes (128 KiB at the published shapes) is
+ *     therefore dynamic shared memory, opted in with
+ *     cudaFuncAttributeMaxDynamicSharedMemorySize up to the device's
+ *     per-block limit.
+ *   num_bins  >= 1
+ *   n         >= 0 (sizes C: small inputs get fewer clusters)
+ *   out       host pointer, filled on success
+ * Errors: EINVAL (bad argument or NULL `out`), EUNSUPPORTED (no cluster shape
+ * can be resident), ECUDA.  Enqueues nothing. */
+DSMEM_HIST_API int dsmem_hist_plan(int32_t num_bins, int64_t n, dsmem_hist_plan_t* out);
+
+/* dsmem_hist_plan with planner overrides (`request` may be NULL), as
+ * dsmem_hist_ex takes them.  The pages have no counterpart: it exists so that
+ * tests and the bench can ask for the exact shape they then force.
  *
  * Every entry point that plans on the current device (dsmem_hist,
- * dsmem_hist_ex, dsmem_hist_host, dsmem_hist_static, dsmem_hist_plan) reads
- * these environment variables for the request fields the caller left to the
- * planner: DSMEM_HIST_CLUSTER (cluster_size), DSMEM_HIST_BLOCK
- * (block_threads), DSMEM_HIST_GRID (num_clusters), DSMEM_HIST_AGGREGATE
- * (aggregate) and DSMEM_HIST_KERNEL (kernel).  DSMEM_HIST_TRACE=1 prints
- * each plan to stderr.  A shape whose clusters cannot be resident falls back
- * from the ship kernel to the direct one, then (unless the cluster size was
- * forced) to smaller clusters. */
-DSMEM_HIST_API int dsmem_hist_plan(int32_t num_bins, int64_t n, const dsmem_hist_request_t* request,
-                    dsmem_hist_plan_t* out);
+ * dsmem_hist_ex, dsmem_hist_host, dsmem_hist_static, dsmem_hist_plan,
+ * dsmem_hist_plan_ex) reads these environment variables for the request
+ * fields the caller left to the planner: DSMEM_HIST_CLUSTER (cluster_size),
+ * DSMEM_HIST_BLOCK (block_threads), DSMEM_HIST_GRID (num_clusters),
+ * DSMEM_HIST_AGGREGATE (aggregate) and DSMEM_HIST_KERNEL (kernel).
+ * DSMEM_HIST_TRACE=1 prints each plan to stderr.  A shape whose clusters
+ * cannot be resident falls back from the ship kernel to the direct one, then
+ * (unless the cluster size was forced) to smaller clusters. */
+DSMEM_HIST_API int dsmem_hist_plan_ex(int32_t num_bins, int64_t n, const dsmem_hist_request_t* request,
+                                      dsmem_hist_plan_t* out);
 
 /* Plan for a described device without touching CUDA (host logic only).
  * `max_active_clusters` is the occupancy answer to use for the chosen shape;

@@ -25,6 +25,17 @@ int main(void) {
   if (dsmem_hist((const int32_t*)bins, -1, 4, bins, NULL) != DSMEM_HIST_EINVAL) return fail("n < 0");
   if (dsmem_hist((const int32_t*)bins, 4, 0, bins, NULL) != DSMEM_HIST_EINVAL) return fail("num_bins");
 
+  /* The planner's plain three-argument form: a NULL `out` is refused before
+   * any CUDA call; with a valid `out` it answers OK on a GPU and an error
+   * code (never a crash) on a machine without one. */
+  dsmem_hist_plan_t here;
+  if (dsmem_hist_plan(262144, (int64_t)1 << 28, NULL) != DSMEM_HIST_EINVAL) return fail("plan NULL out");
+  const int rc_here = dsmem_hist_plan(262144, (int64_t)1 << 28, &here);
+  printf("plan_rc=%d\n", rc_here);
+  if (rc_here != DSMEM_HIST_OK && rc_here != DSMEM_HIST_ECUDA && rc_here != DSMEM_HIST_EUNSUPPORTED)
+    return fail("plan rc");
+  if (rc_here == DSMEM_HIST_OK && here.cluster_size < 2) return fail("plan on this device");
+
   /* The planner for a described GB300: 262,144 bins take clusters of 8
    * CTAs x 32,768 counters in one pass, on the key-shipping kernel. */
   dsmem_hist_device_t dev;
