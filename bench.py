@@ -415,6 +415,30 @@ def run_ours(a, world, rank, local):
     ms_step = ms_total / a.steps
     value = whole_job_rate(world, n, a.steps, ms_total)
 
+    # The product call dsmem_hist itself, timed the same way: it plans (from
+    # the cache), takes its partial rows from the stream-ordered pool, launches
+    # both kernels and returns the rows to the pool, every call.
+    prod_steps = max(1, min(a.steps, 500))
+    prod_out = torch.empty(num_bins, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        pkg.dsmem_hist(keys, num_bins, out=prod_out, stream=stream)
+    torch.cuda.synchronize(dev)
+    ev_start.record(stream)
+    for _ in range(prod_steps):
+        pkg.dsmem_hist(keys, num_bins, out=prod_out, stream=stream)
+    ev_end.record(stream)
+    torch.cuda.synchronize(dev)
+    prod_ms = ev_start.elapsed_time(ev_end) / prod_steps
+    product_call = {"call": "dsmem_hist (planner, pool scratch alloc + free, cluster kernel, "
+                            "reduction)",
+                    "plan": {k: v for k, v in pkg.dsmem_hist_plan(num_bins, n).items()
+                             if k in ("cluster_size", "num_clusters", "kernel", "passes")},
+                    "ms_per_step": prod_ms, "value": world * n / (prod_ms / 1e3), "unit": UNIT,
+                    "steps": prod_steps}
+    if parity is not None:
+        product_call["parity"] = ("bit-exact vs oracle" if np.array_equal(
+            prod_out.cpu().numpy().view(np.uint32), want) else "MISMATCH")
+
     # The global-atomics comparison kernel, timed the same way on the same keys.
     cmp_steps = max(1, min(a.steps, 50))
     for _ in range(3):
@@ -470,8 +494,9 @@ def run_ours(a, world, rank, local):
                      "launch_ms": launch_stats, "share_of_step": cluster_ms / ms_step},
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "product_call": product_call,
         "global_atomic_comparison": comparison,
-        "gpu_launches": 2 * a.steps,
+        "gpu_launches": 2 * a.steps,  # timed region: one cluster kernel + one reduction per step
         "clocks": clocks,
         "parity": parity,
     }

@@ -69,6 +69,18 @@ class TuneResult(ctypes.Structure):
     ]
 
 
+class MicrobenchResult(ctypes.Structure):
+    _fields_ = [
+        ("value", ctypes.c_double),
+        ("ms", ctypes.c_double),
+        ("bytes_per_s", ctypes.c_double),
+        ("ops_expected", ctypes.c_uint64),
+        ("ops_counted", ctypes.c_uint64),
+        ("ctas", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+    ]
+
+
 class Request(ctypes.Structure):
     _fields_ = [
         ("cluster_size", ctypes.c_int32),
@@ -123,8 +135,7 @@ def lib():
                 ("dsmem_hist_ex", [p, i64, i32, p, ctypes.POINTER(Request), p]),
                 ("dsmem_hist_global_atomic", [p, i64, i32, p, p]),
                 ("dsmem_hist_static", [p, i64, i32, p, p]),
-                ("dsmem_hist_microbench", [i32, i32, i32, ctypes.POINTER(ctypes.c_double),
-                                           ctypes.POINTER(ctypes.c_double)]),
+                ("dsmem_hist_microbench", [i32, i32, i32, ctypes.POINTER(MicrobenchResult)]),
                 ("dsmem_hist_tune", [p, i64, i32, i64, i32, ctypes.POINTER(TuneResult),
                                      ctypes.POINTER(i32), p]),
                 ("dsmem_hist_host", [p, i64, i32, p, p]),
@@ -331,21 +342,26 @@ MICROBENCH_KINDS = {
     "cluster_barrier": 4,
     "dsmem_pingpong": 5,
     "gmem_pingpong": 6,
+    "tile_exchange_dsmem": 7,
+    "tile_exchange_gmem": 8,
 }
 
 
 def dsmem_hist_microbench(kind: str, cluster_size: int, iters: int = 4096) -> dict:
     """One DSMEM primitive on the current GPU (see the C header): ops (or
-    bytes) per clock per SM, cycles per cluster barrier, or cycles per
-    one-way ping-pong hop."""
-    value, ms = ctypes.c_double(0), ctypes.c_double(0)
+    bytes) per clock per SM, cycles per cluster barrier, cycles per one-way
+    ping-pong hop, or milliseconds for the tile exchanges; with the work the
+    probe issued (`ops_expected`) and counted on the device (`ops_counted`)."""
+    r = MicrobenchResult()
     _check(lib().dsmem_hist_microbench(MICROBENCH_KINDS[kind], int(cluster_size), int(iters),
-                                       ctypes.byref(value), ctypes.byref(ms)))
+                                       ctypes.byref(r)))
     unit = {"cluster_barrier": "cycles/barrier", "remote_st16_scattered": "bytes/clk/SM",
             "remote_st16_coalesced": "bytes/clk/SM", "dsmem_pingpong": "cycles/hop",
-            "gmem_pingpong": "cycles/hop"}.get(kind, "ops/clk/SM")
-    return {"kind": kind, "cluster_size": cluster_size, "value": value.value, "unit": unit,
-            "ms": ms.value}
+            "gmem_pingpong": "cycles/hop", "tile_exchange_dsmem": "ms",
+            "tile_exchange_gmem": "ms"}.get(kind, "ops/clk/SM")
+    return {"kind": kind, "cluster_size": cluster_size, "iters": iters, "value": r.value,
+            "unit": unit, "ms": r.ms, "bytes_per_s": r.bytes_per_s,
+            "ops_expected": r.ops_expected, "ops_counted": r.ops_counted, "ctas": r.ctas}
 
 
 def dsmem_hist_tune(keys, num_bins: int, sample_keys: int = 0, stream=None) -> list:

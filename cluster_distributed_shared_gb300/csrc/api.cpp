@@ -56,7 +56,16 @@ struct DeviceState {
   // (kernel, variant, threads, smem) -> largest co-schedulable cluster size
   std::map<std::tuple<int, int, int, int>, int> potential;
   std::mutex host_call;  // serialises dsmem_hist_host on this device
+  // Per-stream status words of the ship kernel in pinned, host-mapped memory
+  // (h_status on the host, d_status the same words for the device).
+  uint32_t* h_status = nullptr;
+  uint32_t* d_status = nullptr;
+  std::map<cudaStream_t, int> status_slot;
 };
+
+// Status words per device: one per stream, up to this many streams; later
+// streams share the last word.
+constexpr int kStatusSlots = 64;
 
 std::mutex g_mutex;
 std::map<int, DeviceState*> g_devices;
@@ -100,6 +109,65 @@ int device_state(DeviceState** out) {
   }
   *out = st;
   return DSMEM_HIST_OK;
+}
+
+// Test hooks, read at every call (documented in the header): a shorter
+// bound for the ship kernel's inbox waits, a launch whose senders withhold
+// their last round (so that owners' waits run out with nothing in flight),
+// and a scratch allocation that fails.
+long long wait_cycles_setting() {
+  const char* v = getenv("DSMEM_HIST_TEST_WAIT_CYCLES");
+  if (!v || !*v) return kDefaultWaitCycles;
+  const long long c = atoll(v);
+  return c < 1000 ? 1000 : (c > kDefaultWaitCycles ? kDefaultWaitCycles : c);
+}
+bool env_flag(const char* name) {
+  const char* v = getenv(name);
+  return v && *v && strcmp(v, "0") != 0;
+}
+bool injected_alloc_failure() { return env_flag("DSMEM_HIST_TEST_FAIL_ALLOC"); }
+
+// This stream's status word (host and device views); g_mutex must be held.
+// With may_alloc false, a device whose status words were never allocated
+// gets none (both null).
+int status_word(DeviceState* st, cudaStream_t stream, bool may_alloc, uint32_t** h, uint32_t** d) {
+  *h = *d = nullptr;
+  if (!st->h_status) {
+    if (!may_alloc) return DSMEM_HIST_OK;
+    void* p = nullptr;
+    cudaError_t e = cudaHostAlloc(&p, kStatusSlots * sizeof(uint32_t),
+                                  cudaHostAllocMapped | cudaHostAllocPortable);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaHostAlloc (status words)");
+    memset(p, 0, kStatusSlots * sizeof(uint32_t));
+    void* dp = nullptr;
+    if ((e = cudaHostGetDevicePointer(&dp, p, 0)) != cudaSuccess) {
+      cudaFreeHost(p);
+      return fail_cuda(e, "cudaHostGetDevicePointer (status words)");
+    }
+    st->h_status = static_cast<uint32_t*>(p);
+    st->d_status = static_cast<uint32_t*>(dp);
+  }
+  auto it = st->status_slot.find(stream);
+  int slot;
+  if (it != st->status_slot.end()) {
+    slot = it->second;
+  } else {
+    slot = std::min<int>(static_cast<int>(st->status_slot.size()), kStatusSlots - 1);
+    st->status_slot[stream] = slot;
+  }
+  *h = st->h_status + slot;
+  *d = st->d_status + slot;
+  return DSMEM_HIST_OK;
+}
+
+// Reports (once) a bounded wait that gave up in an earlier launch on this
+// stream, as seen from the host without synchronising.
+int take_pending_timeout(uint32_t* h) {
+  if (!h || *reinterpret_cast<volatile uint32_t*>(h) == 0u) return DSMEM_HIST_OK;
+  *reinterpret_cast<volatile uint32_t*>(h) = 0u;
+  return fail(DSMEM_HIST_ETIMEOUT,
+              "an earlier ship-kernel launch on this stream had a bounded inbox wait give up, so "
+              "its histogram was wrong; this call enqueued nothing (call again)");
 }
 
 int ensure_pool(DeviceState* st) {
@@ -267,6 +335,9 @@ ClusterHistArgs make_args(const dsmem_hist_plan_t& plan, const int32_t* keys, in
   a.head = head_keys(keys, n);
   a.accumulate = static_cast<uint32_t>(accumulate);
   a.sub_vectors = static_cast<uint32_t>(plan.sub_vectors);
+  a.status = nullptr;
+  a.wait_cycles = wait_cycles_setting();
+  a.withhold_last = env_flag("DSMEM_HIST_TEST_WITHHOLD_LAST_ROUND") ? 1u : 0u;
   return a;
 }
 
@@ -276,9 +347,12 @@ int run_device(const int32_t* keys, int64_t n, int32_t num_bins, uint32_t* bins,
   if (rc) return rc;
   dsmem_hist_plan_t plan;
   DeviceState* st = nullptr;
+  uint32_t *h_status = nullptr, *d_status = nullptr;
   {
     std::lock_guard<std::mutex> g(g_mutex);
     if ((rc = device_state(&st))) return rc;
+    if ((rc = status_word(st, stream, true, &h_status, &d_status))) return rc;
+    if ((rc = take_pending_timeout(h_status))) return rc;
     if ((rc = plan_locked(st, num_bins, n, req, &plan))) return rc;
     if ((rc = ensure_pool(st))) return rc;
   }
@@ -287,6 +361,9 @@ int run_device(const int32_t* keys, int64_t n, int32_t num_bins, uint32_t* bins,
     e = cudaMemsetAsync(bins, 0, sizeof(uint32_t) * static_cast<size_t>(num_bins), stream);
     return e == cudaSuccess ? DSMEM_HIST_OK : fail_cuda(e, "cudaMemsetAsync");
   }
+  if (injected_alloc_failure())
+    return fail(DSMEM_HIST_ENOMEM, "scratch pool: %lld bytes: allocation failure injected by "
+                "DSMEM_HIST_TEST_FAIL_ALLOC", static_cast<long long>(plan.workspace_bytes));
   void* scratch = nullptr;
   e = cudaMallocFromPoolAsync(&scratch, static_cast<size_t>(plan.workspace_bytes), st->pool, stream);
   if (e != cudaSuccess) {
@@ -295,7 +372,8 @@ int run_device(const int32_t* keys, int64_t n, int32_t num_bins, uint32_t* bins,
                 static_cast<long long>(plan.workspace_bytes), cudaGetErrorString(e));
   }
   uint32_t* partials = static_cast<uint32_t*>(scratch);
-  const ClusterHistArgs args = make_args(plan, keys, n, num_bins, partials, 0);
+  ClusterHistArgs args = make_args(plan, keys, n, num_bins, partials, 0);
+  args.status = d_status;
   e = launch_plan(plan, args, stream);
   if (e == cudaSuccess)
     e = launch_reduce_partials(partials, args.stride, static_cast<uint32_t>(plan.num_clusters),
@@ -343,6 +421,7 @@ int run_partials(const int32_t* keys, int64_t n, int32_t num_bins, const dsmem_h
   if (reinterpret_cast<uintptr_t>(partials) & 15u)
     return fail(DSMEM_HIST_EINVAL, "partials must be 16-byte aligned");
   if (accumulate != 0 && accumulate != 1) return fail(DSMEM_HIST_EINVAL, "accumulate must be 0 or 1");
+  uint32_t *h_status = nullptr, *d_status = nullptr;
   {
     std::lock_guard<std::mutex> g(g_mutex);
     DeviceState* st = nullptr;
@@ -350,9 +429,12 @@ int run_partials(const int32_t* keys, int64_t n, int32_t num_bins, const dsmem_h
     if ((rc = check_plan(st, plan, num_bins))) return rc;
     if (plan->kernel == DSMEM_HIST_KERNEL_SHIP && n >= kShipMaxKeys)
       return fail(DSMEM_HIST_EINVAL, "the ship kernel takes fewer than 2^38 keys per call");
+    if ((rc = status_word(st, stream, true, &h_status, &d_status))) return rc;
+    if ((rc = take_pending_timeout(h_status))) return rc;
     if ((rc = prepare_locked(st, *plan))) return rc;
   }
-  const ClusterHistArgs args = make_args(*plan, keys, n, num_bins, partials, accumulate);
+  ClusterHistArgs args = make_args(*plan, keys, n, num_bins, partials, accumulate);
+  args.status = d_status;
   const cudaError_t e = launch_plan(*plan, args, stream);
   return e == cudaSuccess ? DSMEM_HIST_OK : fail_cuda(e, "cluster histogram launch");
 }
@@ -381,9 +463,12 @@ int run_host(const int32_t* h_keys, int64_t n, int32_t num_bins, uint32_t* h_bin
   DeviceState* st = nullptr;
   dsmem_hist_plan_t plan;
   const int64_t chunk = n < kHostChunkKeys ? n : kHostChunkKeys;
+  uint32_t *h_status = nullptr, *d_status = nullptr;
   {
     std::lock_guard<std::mutex> g(g_mutex);
     if ((rc = device_state(&st))) return rc;
+    if ((rc = status_word(st, stream, true, &h_status, &d_status))) return rc;
+    if ((rc = take_pending_timeout(h_status))) return rc;
     if ((rc = plan_locked(st, num_bins, chunk, nullptr, &plan))) return rc;
     if ((rc = ensure_pool(st))) return rc;
     cudaError_t e;
@@ -404,6 +489,9 @@ int run_host(const int32_t* h_keys, int64_t n, int32_t num_bins, uint32_t* h_bin
   const size_t chunk_bytes = ((sizeof(int32_t) * static_cast<size_t>(chunk)) + 255) & ~size_t{255};
   const size_t total = bins_alloc + static_cast<size_t>(plan.workspace_bytes) + 2 * chunk_bytes;
   void* scratch = nullptr;
+  if (injected_alloc_failure())
+    return fail(DSMEM_HIST_ENOMEM, "scratch pool: %zu bytes: allocation failure injected by "
+                "DSMEM_HIST_TEST_FAIL_ALLOC", total);
   if ((e = cudaMallocFromPoolAsync(&scratch, total, st->pool, stream)) != cudaSuccess) {
     cudaGetLastError();
     return fail(DSMEM_HIST_ENOMEM, "scratch pool: %zu bytes: %s", total, cudaGetErrorString(e));
@@ -435,7 +523,8 @@ int run_host(const int32_t* h_keys, int64_t n, int32_t num_bins, uint32_t* h_bin
       rc = fail_cuda(e, "staging copy");
       break;
     }
-    const ClusterHistArgs args = make_args(plan, stage[b], cnt, num_bins, partials, j > 0);
+    ClusterHistArgs args = make_args(plan, stage[b], cnt, num_bins, partials, j > 0);
+    args.status = d_status;
     if ((e = launch_plan(plan, args, stream)) != cudaSuccess ||
         (e = cudaEventRecord(st->ev_consumed[b], stream)) != cudaSuccess) {
       rc = fail_cuda(e, "cluster histogram launch");
@@ -477,15 +566,30 @@ int run_with_fixed_scratch(const int32_t* keys, int64_t n, int32_t num_bins, uin
                 num_bins, static_cast<long long>(row_bytes), static_cast<long long>(max_rows_bytes),
                 static_cast<long long>(max_rows_bytes / 4));
   dsmem_hist_plan_t plan;
+  uint32_t *h_status = nullptr, *d_status = nullptr;
   {
     std::lock_guard<std::mutex> g(g_mutex);
     DeviceState* st = nullptr;
     if ((rc = device_state(&st))) return rc;
+    // Status words only if an earlier call already allocated them: this path
+    // allocates nothing.
+    if ((rc = status_word(st, stream, false, &h_status, &d_status))) return rc;
+    if ((rc = take_pending_timeout(h_status))) return rc;
     if ((rc = plan_locked(st, num_bins, n, nullptr, &plan))) return rc;
     if (plan.workspace_bytes > max_rows_bytes) {
-      // Fewer clusters, so their partial rows fit the static scratch.
+      // Fewer clusters, so their partial rows fit the static scratch.  The
+      // forced count is below the automatic one (whose rows did not fit), so
+      // it never exceeds the clusters that can be resident or the rows the
+      // scratch holds.
+      const int32_t auto_clusters = plan.num_clusters;
       dsmem_hist_request_t req = {0, 0, static_cast<int32_t>(max_rows_bytes / row_bytes), -1, 0, -1};
+      if (req.num_clusters >= auto_clusters || req.num_clusters < 1)
+        return fail(DSMEM_HIST_EINVAL, "static scratch: %d rows of %lld bytes do not fit below the "
+                    "automatic %d clusters", req.num_clusters, static_cast<long long>(row_bytes),
+                    auto_clusters);
       if ((rc = plan_locked(st, num_bins, n, &req, &plan))) return rc;
+      if (plan.num_clusters > req.num_clusters || plan.workspace_bytes > max_rows_bytes)
+        return fail(DSMEM_HIST_EINVAL, "static scratch: forced plan exceeds the scratch");
     }
   }
   cudaError_t e;
@@ -493,7 +597,8 @@ int run_with_fixed_scratch(const int32_t* keys, int64_t n, int32_t num_bins, uin
     e = cudaMemsetAsync(bins, 0, sizeof(uint32_t) * static_cast<size_t>(num_bins), stream);
     return e == cudaSuccess ? DSMEM_HIST_OK : fail_cuda(e, "cudaMemsetAsync");
   }
-  const ClusterHistArgs args = make_args(plan, keys, n, num_bins, scratch, 0);
+  ClusterHistArgs args = make_args(plan, keys, n, num_bins, scratch, 0);
+  args.status = d_status;
   e = launch_plan(plan, args, stream);
   if (e == cudaSuccess)
     e = launch_reduce_partials(scratch, args.stride, static_cast<uint32_t>(plan.num_clusters),
@@ -583,6 +688,9 @@ int run_tune(const int32_t* keys, int64_t n, int32_t num_bins, int64_t sample_ke
   for (const auto& c : cand) ws = std::max(ws, c.plan.workspace_bytes);
   const size_t bins_bytes = (4 * static_cast<size_t>(num_bins) + 255) & ~size_t{255};
   void* scratch = nullptr;
+  if (injected_alloc_failure())
+    return fail(DSMEM_HIST_ENOMEM, "tune scratch: allocation failure injected by "
+                "DSMEM_HIST_TEST_FAIL_ALLOC");
   cudaError_t e = cudaMallocFromPoolAsync(&scratch, bins_bytes + static_cast<size_t>(ws) + 256,
                                           st->pool, stream);
   if (e != cudaSuccess) {
@@ -723,6 +831,12 @@ void dsmem_hist_release(void) {
       cudaDeviceSynchronize();
       cudaMemPoolDestroy(st->pool);
       st->pool = nullptr;
+    }
+    if (st->h_status) {
+      cudaDeviceSynchronize();
+      cudaFreeHost(st->h_status);
+      st->h_status = st->d_status = nullptr;
+      st->status_slot.clear();
     }
     if (st->copy_stream) {
       cudaStreamDestroy(st->copy_stream);

@@ -198,19 +198,22 @@ __device__ __forceinline__ void apply_vector(uint32_t slice, const uint4& x) {
 
 __device__ uint32_t g_ship_status;  // bit 0: a bounded wait gave up (until read and cleared)
 
-// Waits for phase `parity` of an inbox mbarrier, at most ~1e8 cycles
-// (~50 ms).  On a timeout the device status word records it, this CTA's
-// shared flag at `gave_up` is set, and the caller skips the buffer; once a wait of
-// this CTA has timed out, its later waits in the same launch give up after
-// one probe.  Later launches start with the flag clear.
-__device__ __forceinline__ bool wait_inbox(uint32_t mbar, uint32_t parity, uint32_t gave_up) {
+// Waits for phase `parity` of an inbox mbarrier, at most `limit` cycles
+// (by default ~1e8, about 50 ms).  On a timeout the device status word and
+// the call's host-mapped word (if any) record it, this CTA's shared flag at
+// `gave_up` is set, and the caller skips the buffer; once a wait of this CTA
+// has timed out, its later waits in the same launch give up after one probe.
+// Later launches start with the flag clear.
+__device__ __forceinline__ bool wait_inbox(uint32_t mbar, uint32_t parity, uint32_t gave_up,
+                                           long long limit, uint32_t* status) {
   if (mbar_try_wait(mbar, parity)) return true;
   if (ld_shared_u32(gave_up) != 0u) return false;
-  const long long deadline = clock64() + 100000000ll;
+  const long long deadline = clock64() + limit;
   while (clock64() < deadline)
     if (mbar_try_wait(mbar, parity)) return true;
   st_shared_u32(gave_up, 1u);
   atomicOr(&g_ship_status, 1u);
+  if (status) st_volatile_u32(status, 1u);
   return false;
 }
 
@@ -355,7 +358,7 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
         // arrived and every byte has landed (this CTA's own block was
         // applied straight from staging when it was shipped).
         const uint32_t pb = b ^ 1u;
-        if (wait_inbox(full0 + 8u * pb, ((r - 1u) >> 1) & 1u, gave_up)) {
+        if (wait_inbox(full0 + 8u * pb, ((r - 1u) >> 1) & 1u, gave_up, a.wait_cycles, a.status)) {
           const uint32_t src = src0 + pb * buf_bytes;
           const uint32_t end = src - vofs + 64u * min(ld_shared_u32(hdr_in + 64u * pb), qs);
           for (uint32_t at = src; at < end; at += step) apply_vector(c.slice, ld_shared_v4(at));
@@ -381,7 +384,7 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
             apply_vector(c.slice, ld_shared_v4(at));
             st_shared_v4(at, pad);
           }
-        } else {
+        } else if (!(a.withhold_last && r + 1u == rounds)) {
           const uint32_t mbar = full_out + 8u * b;
           if (sg == 0 && c.lane == 0) {
             mbar_arrive_expect_tx_remote(mbar, 64u * rows + 4u);
@@ -409,7 +412,7 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
     }
     if (rounds > 0 && so != rank) {
       const uint32_t pb = (rounds - 1u) & 1u;
-      if (wait_inbox(full0 + 8u * pb, ((rounds - 1u) >> 1) & 1u, gave_up)) {
+      if (wait_inbox(full0 + 8u * pb, ((rounds - 1u) >> 1) & 1u, gave_up, a.wait_cycles, a.status)) {
         const uint32_t src = src0 + pb * buf_bytes;
         const uint32_t end = src - vofs + 64u * min(ld_shared_u32(hdr_in + 64u * pb), qs);
         for (uint32_t at = src; at < end; at += step) apply_vector(c.slice, ld_shared_v4(at));
@@ -433,6 +436,17 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
     }
 
     cluster_barrier();  // every increment has landed; only own memory after this
+    if (ld_shared_u32(gave_up) != 0u) {
+      // A wait of this CTA gave up, so an inbox phase may be incomplete.
+      // Every sender has issued all its stores (it reached the barrier
+      // above), but only the mbarrier tracks their delivery: give bytes still
+      // in flight a bounded grace period (DSMEM delivery takes about a
+      // microsecond) before the mbarriers are invalidated and the CTA leaves.
+      const long long grace = a.wait_cycles < (1ll << 22) ? a.wait_cycles : (1ll << 22);
+      const long long until = clock64() + grace;
+      while (clock64() < until) {
+      }
+    }
     if (threadIdx.x == 0) {
       mbar_inval(full0);
       mbar_inval(full0 + 8u);

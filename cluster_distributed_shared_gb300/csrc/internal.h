@@ -46,7 +46,17 @@ struct ClusterHistArgs {
   uint32_t head;        // keys before the first 16-byte boundary of `keys` (0..3, <= n)
   uint32_t accumulate;  // 1: add the slice into the partial row, 0: overwrite it
   uint32_t sub_vectors; // ship kernel: rows of each owner's staging block
+  // Ship kernel error channel and wait bound.  `status` (may be null) is this
+  // call's word in pinned, host-mapped memory: a bounded inbox wait that gives
+  // up sets bit 0 there (and in the device-wide status word), so the next call
+  // on the same stream can report it without a device synchronisation.
+  uint32_t* status;
+  long long wait_cycles;    // bound of one inbox wait (clock64 cycles)
+  uint32_t withhold_last;   // test only: senders skip the last round's arrival and stores
 };
+
+// Default bound of one inbox wait: ~1e8 cycles, about 50 ms at 2 GHz.
+constexpr long long kDefaultWaitCycles = 100000000ll;
 
 // Launches (all asynchronous on `stream`).
 cudaError_t launch_cluster_hist(const dsmem_hist_plan_t& plan, const ClusterHistArgs& args,

@@ -29,6 +29,32 @@
  *     and is returned to the pool on the same stream, so calls on different
  *     streams never share scratch.
  *   - Thread-safe: the per-device state is guarded by a mutex.
+ *   - Device-side failures (no counterpart in the pages' design, which waits
+ *     only on cluster barriers): the key-shipping kernel waits for its peers'
+ *     inbox bytes with bounded waits (about 50 ms each).  A wait that gives
+ *     up skips that inbox (the launch's histogram is then wrong) and records
+ *     the failure in two places: a word for the call's stream in pinned,
+ *     host-mapped memory, and the device-wide status word.  The first
+ *     histogram call on the same stream that starts after the failing launch
+ *     has finished returns DSMEM_HIST_ETIMEOUT and enqueues nothing (call it
+ *     again); dsmem_hist_device_status() reads and clears the device-wide
+ *     word.  The host-mapped words (64 streams per device; later streams
+ *     share the last word) are allocated by the first dsmem_hist,
+ *     dsmem_hist_ex, dsmem_hist_host or dsmem_hist_partials call on a device;
+ *     dsmem_hist_static, which allocates nothing, uses them only if they
+ *     exist already and otherwise reports through the device-wide word alone.
+ *   - Test hooks, read from the environment at every call (for tests of the
+ *     failure paths above; leave them unset otherwise):
+ *       DSMEM_HIST_TEST_WAIT_CYCLES=c           bound one inbox wait to c clock
+ *                                               cycles (1000 .. 1e8)
+ *       DSMEM_HIST_TEST_WITHHOLD_LAST_ROUND=1   the key-shipping kernel's senders
+ *                                               skip their last round's arrival
+ *                                               and stores, so owners' last waits
+ *                                               run out with nothing in flight
+ *       DSMEM_HIST_TEST_FAIL_ALLOC=1            scratch allocations of dsmem_hist,
+ *                                               dsmem_hist_ex, dsmem_hist_host and
+ *                                               dsmem_hist_tune fail with
+ *                                               DSMEM_HIST_ENOMEM
  */
 #ifndef DSMEM_HIST_H
 #define DSMEM_HIST_H
@@ -51,7 +77,7 @@ enum {
   DSMEM_HIST_EINVAL = -1,       /* bad argument (null pointer with n > 0, n < 0, num_bins < 1, misaligned) */
   DSMEM_HIST_EUNSUPPORTED = -2, /* device below compute capability 9.0, or no legal cluster shape */
   DSMEM_HIST_ECUDA = -3,        /* a CUDA runtime call or kernel launch failed */
-  DSMEM_HIST_ETIMEOUT = -4,     /* a bounded device-side wait gave up (reported by a later sync) */
+  DSMEM_HIST_ETIMEOUT = -4,     /* a bounded device-side wait of an earlier launch gave up (see below) */
   DSMEM_HIST_ENOMEM = -5        /* the scratch pool could not supply the partial histograms */
 };
 
@@ -117,7 +143,9 @@ typedef struct dsmem_hist_device {
  *   bins     device, num_bins uint32 (overwritten)
  *   stream   CUDA stream the work is enqueued on
  * Errors: EINVAL for bad arguments (nothing enqueued), EUNSUPPORTED, ECUDA,
- * ENOMEM. */
+ * ENOMEM (the scratch pool could not supply the partial rows; nothing
+ * enqueued), ETIMEOUT (an earlier launch on this stream had a wait give up;
+ * nothing enqueued). */
 DSMEM_HIST_API int dsmem_hist(const int32_t* keys, int64_t n, int32_t num_bins, uint32_t* bins,
                cudaStream_t stream);
 
@@ -221,28 +249,56 @@ enum {
   DSMEM_HIST_MB_REMOTE_ST16_COALESCED = 3, /* st.shared::cluster.v4, 512 contiguous bytes per warp */
   DSMEM_HIST_MB_CLUSTER_BARRIER = 4,       /* barrier.cluster arrive + wait */
   DSMEM_HIST_MB_DSMEM_PINGPONG = 5,        /* one-way latency of a flag in a peer CTA's shared memory */
-  DSMEM_HIST_MB_GMEM_PINGPONG = 6          /* one-way latency of a flag in global memory */
+  DSMEM_HIST_MB_GMEM_PINGPONG = 6,         /* one-way latency of a flag in global memory */
+  DSMEM_HIST_MB_TILE_EXCHANGE_DSMEM = 7,   /* 16 KB tile pulled from the pair CTA's shared memory */
+  DSMEM_HIST_MB_TILE_EXCHANGE_GMEM = 8     /* 16 KB tile exchanged through a global scratch + fence */
 };
 
+/* One microbenchmark's answer. */
+typedef struct dsmem_hist_microbench_result {
+  double value;          /* rate kinds (0..3): operations per clock per SM (bytes per clock
+                            per SM for the two store kinds); barrier kind: clock cycles per
+                            barrier; ping-pong kinds: clock cycles per one-way hop (half a
+                            round trip); tile-exchange kinds: milliseconds for all iterations */
+  double ms;             /* CUDA-event time of the timed launch */
+  double bytes_per_s;    /* tile-exchange kinds: tile bytes landed per second, counted once
+                            (every CTA receives one 16 KiB tile per iteration); 0 otherwise */
+  uint64_t ops_expected; /* the work the probe issues by construction (see below) */
+  uint64_t ops_counted;  /* the same work as counted on the device after the closing barrier */
+  int32_t ctas;          /* CTAs launched (tile-exchange kinds; 0 otherwise) */
+  int32_t reserved;      /* zero */
+} dsmem_hist_microbench_result_t;
+
 /* Measures one DSMEM primitive on the current GPU ("Hopper DSMEM vs HBM",
- * tile-exchange and ping-pong sections; "CREDIT", microbenchmark section).
- * Rate kinds (0..4): 1024 threads per CTA, 128 KiB of shared memory per CTA,
- * every resident cluster of `cluster_size` CTAs, `iters` operations per
- * thread.  Ping-pong kinds (5, 6): one cluster of `cluster_size` >= 2 CTAs;
- * one thread of CTA 0 and one of CTA 1 pass a counter back and forth `iters`
- * times through a flag in the receiver's shared memory (written with a
- * release store to shared::cluster, read with acquire loads) or in global
- * memory (release/acquire at GPU scope), as the page's ping-pong test does.
- * Every wait for the peer is bounded (2^20 polls); a wait that gives up ends
- * the test with DSMEM_HIST_ETIMEOUT.
- *   *value  operations per clock per SM (bytes per clock per SM for the two
- *           store kinds; clock cycles per barrier for the barrier kind;
- *           clock cycles per one-way hop, half a round trip, for ping-pong)
- *   *ms     wall time of the timed launch
- * Synchronous; allocates and frees its own small device buffers.  With
- * cluster_size 1 the "remote" rate kinds address this CTA itself. */
+ * the ping-pong test and the 16 KB tile-exchange test; "CREDIT",
+ * microbenchmark section).  One warm-up launch, then the timed launch.
+ *   Rate kinds (0..4): 1024 threads per CTA, 128 KiB of shared memory per
+ *     CTA, every resident cluster of `cluster_size` CTAs, `iters` operations
+ *     per thread, timed with clock64 per CTA.  With cluster_size 1 the
+ *     "remote" kinds address this CTA itself.
+ *   Ping-pong kinds (5, 6): one cluster of `cluster_size` >= 2 CTAs; one
+ *     thread of CTA 0 and one of CTA 1 pass a counter back and forth `iters`
+ *     times through a flag in the receiver's shared memory (written with a
+ *     release store to shared::cluster, read with acquire loads) or in global
+ *     memory (release/acquire at GPU scope).  Every wait for the peer is
+ *     bounded (2^20 polls); a wait that gives up ends the test with
+ *     DSMEM_HIST_ETIMEOUT.
+ *   Tile-exchange kinds (7, 8): every resident cluster of an even
+ *     `cluster_size` (the page uses 2), 128 threads per CTA, one CTA per SM.
+ *     CTAs 2j and 2j+1 of a cluster each own a 16 KiB tile of 4096 32-bit
+ *     words in shared memory, and every iteration lands the other's tile in
+ *     its own shared memory: kind 7 pulls it through the cluster address of
+ *     the peer's tile and meets one cluster barrier; kind 8 writes its tile
+ *     to a global scratch, fences, meets the barrier, reads the peer's slot
+ *     from L2 and meets the barrier again.
+ * Counted work (ops_expected against ops_counted, equal when the probe did
+ * what it claims): the two reduction kinds count the increments that landed
+ * in the slices; the store and barrier kinds the operations every thread
+ * issued; the ping-pong kinds the completed round trips; the tile-exchange
+ * kinds the sum of every word pulled from the peer over all iterations.
+ * Synchronous; allocates and frees its own small device buffers. */
 DSMEM_HIST_API int dsmem_hist_microbench(int32_t kind, int32_t cluster_size, int32_t iters,
-                                         double* value, double* ms);
+                                         dsmem_hist_microbench_result_t* out);
 
 /* The launch shape dsmem_hist would use on the current device for num_bins
  * bins and n keys: cluster size P, counters per CTA S, passes, threads per
@@ -314,12 +370,14 @@ DSMEM_HIST_API void dsmem_hist_release(void);
 /* Reads and clears the current device's status word of the key-shipping
  * kernel (DSMEM_HIST_KERNEL_SHIP).  That kernel waits for its peers' inbox
  * bytes with bounded waits (about 50 ms each); a wait that gives up sets bit 0
- * of the word and skips that inbox, so the histogram of that launch is wrong.
- * *status (may be NULL) receives the word.  Synchronous: it reads the word
- * with cudaMemcpyFromSymbol on the legacy default stream.  Returns
- * DSMEM_HIST_OK if the word was 0, DSMEM_HIST_ETIMEOUT if a wait gave up since
- * the last call, DSMEM_HIST_ECUDA on a CUDA error.  No counterpart in the
- * pages' design, which waits only on cluster barriers. */
+ * of the word (and of the calling stream's host-mapped word, see the
+ * conventions at the top) and skips that inbox, so the histogram of that
+ * launch is wrong.  *status (may be NULL) receives the word.  Reads with
+ * cudaMemcpyFromSymbol, which is ordered with the legacy default stream only:
+ * synchronise the streams of interest first.  Returns DSMEM_HIST_OK if the
+ * word was 0, DSMEM_HIST_ETIMEOUT if a wait gave up since the last call,
+ * DSMEM_HIST_ECUDA on a CUDA error.  No counterpart in the pages' design,
+ * which waits only on cluster barriers. */
 DSMEM_HIST_API int dsmem_hist_device_status(uint32_t* status);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */

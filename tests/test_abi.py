@@ -259,13 +259,17 @@ def test_tune_and_microbench_reject_bad_arguments():
     res = (pkg.TuneResult * 2)()
     assert L.dsmem_hist_tune(p, -1, 8, 0, 2, res, ctypes.byref(count), None) == pkg.DSMEM_HIST_EINVAL
     assert L.dsmem_hist_tune(p, 4, 0, 0, 2, res, ctypes.byref(count), None) == pkg.DSMEM_HIST_EINVAL
-    v, ms = ctypes.c_double(), ctypes.c_double()
-    assert L.dsmem_hist_microbench(0, 17, 16, ctypes.byref(v), ctypes.byref(ms)) == pkg.DSMEM_HIST_EINVAL
-    assert L.dsmem_hist_microbench(0, 2, 0, ctypes.byref(v), ctypes.byref(ms)) == pkg.DSMEM_HIST_EINVAL
+    r = ctypes.byref(pkg.MicrobenchResult())
+    assert L.dsmem_hist_microbench(0, 17, 16, r) == pkg.DSMEM_HIST_EINVAL
+    assert L.dsmem_hist_microbench(0, 2, 0, r) == pkg.DSMEM_HIST_EINVAL
+    assert L.dsmem_hist_microbench(0, 2, 16, None) == pkg.DSMEM_HIST_EINVAL
     # ping-pong needs two CTAs and a bounded number of rounds
-    assert L.dsmem_hist_microbench(5, 1, 16, ctypes.byref(v), ctypes.byref(ms)) == pkg.DSMEM_HIST_EINVAL
-    assert L.dsmem_hist_microbench(6, 2, (1 << 20) + 1, ctypes.byref(v), ctypes.byref(ms)) == \
-        pkg.DSMEM_HIST_EINVAL
+    assert L.dsmem_hist_microbench(5, 1, 16, r) == pkg.DSMEM_HIST_EINVAL
+    assert L.dsmem_hist_microbench(6, 2, (1 << 20) + 1, r) == pkg.DSMEM_HIST_EINVAL
+    # the tile exchange pairs CTAs 2j and 2j + 1: an even cluster size
+    assert L.dsmem_hist_microbench(7, 3, 16, r) == pkg.DSMEM_HIST_EINVAL
+    assert L.dsmem_hist_microbench(8, 1, 16, r) == pkg.DSMEM_HIST_EINVAL
+    assert L.dsmem_hist_microbench(9, 2, 16, r) == pkg.DSMEM_HIST_EINVAL
 
 
 def test_ship_threads_match_header():

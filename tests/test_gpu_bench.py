@@ -76,3 +76,12 @@ def test_clock_record_is_present(line):
     clocks = line["clocks"]
     assert isinstance(clocks, dict)
     assert "sm_mhz" in clocks and "sm_max_mhz" in clocks and "reasons" in clocks
+
+
+@pytest.mark.gpu
+def test_product_call_is_timed_and_exact(line):
+    p = line["product_call"]
+    assert p["call"].startswith("dsmem_hist") and p["steps"] >= 1
+    assert p["parity"] == "bit-exact vs oracle"
+    assert p["value"] == pytest.approx(N / (p["ms_per_step"] / 1e3), rel=1e-6)
+    assert p["unit"] == line["unit"] and p["plan"]["cluster_size"] >= 2

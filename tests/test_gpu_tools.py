@@ -43,21 +43,43 @@ def test_tune_ranks_every_shape_and_its_winner_is_exact(num_bins):
         assert np.array_equal(got.cpu().numpy().view(np.uint32), want), r
 
 
-def test_microbench_rates_are_consistent():
-    rates = {k: pkg.dsmem_hist_microbench(k, 2, iters=512)
-             for k in pkg.MICROBENCH_KINDS}
+def test_microbench_rates_are_consistent_and_did_their_counted_work():
+    kinds = [k for k in pkg.MICROBENCH_KINDS if not k.startswith("tile_exchange")]
+    rates = {k: pkg.dsmem_hist_microbench(k, 2, iters=512) for k in kinds}
+    for k, r in rates.items():
+        # every probe did exactly the work it claims: increments landed,
+        # stores and barriers issued, round trips completed
+        assert r["ops_counted"] == r["ops_expected"] > 0, r
+        assert r["value"] > 0 and r["ms"] > 0, r
+    assert rates["dsmem_pingpong"]["ops_expected"] == 512
     # one-way flag latency: hundreds to thousands of cycles, and a flag in a
     # peer's shared memory arrives no later than one in global memory
     for k in ("dsmem_pingpong", "gmem_pingpong"):
         assert 20 < rates[k]["value"] < 1e5, rates[k]
     assert rates["dsmem_pingpong"]["value"] < 1.5 * rates["gmem_pingpong"]["value"]
-    for r in rates.values():
-        assert r["value"] > 0 and r["ms"] > 0
     # a local shared-memory atomic is far cheaper than a remote one
     assert rates["local_red"]["value"] > 4 * rates["remote_red"]["value"]
     # one cluster barrier costs at least tens of cycles and well under a million
     assert 10 < rates["cluster_barrier"]["value"] < 1e6
+    # the same counts hold at the other cluster sizes the histogram uses
+    for P in (1, 8, 16):
+        for k in ("local_red", "remote_red", "remote_st16_coalesced", "cluster_barrier"):
+            r = pkg.dsmem_hist_microbench(k, P, iters=64)
+            assert r["ops_counted"] == r["ops_expected"] > 0, r
     import ctypes
-    v, ms = ctypes.c_double(), ctypes.c_double()
-    assert pkg.lib().dsmem_hist_microbench(99, 2, 16, ctypes.byref(v), ctypes.byref(ms)) == \
-        pkg.DSMEM_HIST_EINVAL
+    res = pkg.MicrobenchResult()
+    assert pkg.lib().dsmem_hist_microbench(99, 2, 16, ctypes.byref(res)) == pkg.DSMEM_HIST_EINVAL
+
+
+@pytest.mark.parametrize("P", [2, 4])
+def test_tile_exchange_pair_moves_every_tile(P):
+    iters = 500
+    d = pkg.dsmem_hist_microbench("tile_exchange_dsmem", P, iters=iters)
+    g = pkg.dsmem_hist_microbench("tile_exchange_gmem", P, iters=iters)
+    for r in (d, g):
+        # every word of the peer's tile arrived on every iteration
+        assert r["ops_counted"] == r["ops_expected"] > 0, r
+        assert r["ctas"] >= 2 * P and r["ctas"] % P == 0
+        assert r["value"] == r["ms"] > 0
+        assert r["bytes_per_s"] == pytest.approx(r["ctas"] * 16384 * iters / (r["ms"] * 1e-3))
+    assert d["ctas"] == g["ctas"]
