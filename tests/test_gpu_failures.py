@@ -78,7 +78,7 @@ def test_inbox_wait_runs_out_and_the_next_call_reports_it(monkeypatch, fn):
     # The same stream: the next call reports the timeout once and enqueues nothing.
     sentinel = torch.full((num_bins,), 7, dtype=torch.int32, device="cuda")
     assert _call(fn, keys, num_bins, sentinel, s) == pkg.DSMEM_HIST_ETIMEOUT
-    assert b"gave up" in pkg.lib().dsmem_hist_last_error()
+    assert b"wait give up" in pkg.lib().dsmem_hist_last_error()
     s.synchronize()
     assert (sentinel == 7).all().item()
     assert _call(fn, keys, num_bins, out, s) == pkg.DSMEM_HIST_OK
