@@ -41,6 +41,7 @@ WORKLOAD_CLUSTER = {
     "uniform-256M-256K": 8,
     "zipf1.1-256M-256K": 8,
     "runs256-1G-512K": 16,
+    "hot25-256M-256K": 8,   # skewed case: a quarter of the keys on one bin
 }
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
@@ -71,6 +72,8 @@ def parse():
                          "smaller cases; default: the workload's own length)")
     ap.add_argument("--cluster", type=int, default=0,
                     help="cluster size (default: the workload's published one)")
+    ap.add_argument("--hot-bin-hint", action="store_true",
+                    help="hot25 workload: tell the library its hot bin (the hinted ship kernel)")
     a = ap.parse_args()
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -348,7 +351,13 @@ def run_ours(a, world, rank, local):
     n, num_bins, P = cfg["n"], cfg["num_bins"], cfg["cluster_size"]
     keys_h = gen.workload(a.workload, seed, n=cfg["n"])
     keys = torch.from_numpy(keys_h).to(dev)
-    plan = pkg.dsmem_hist_plan(num_bins, n, cluster_size=P)
+    hint = {}
+    if a.hot_bin_hint:
+        if gen.WORKLOADS[a.workload]["dist"] != "hot":
+            raise SystemExit("--hot-bin-hint applies to the hot25 workload only")
+        hint = {"hot_bin": gen.hot_bin(num_bins, seed)}
+        cfg["hot_bin_hint"] = hint["hot_bin"]
+    plan = pkg.dsmem_hist_plan(num_bins, n, cluster_size=P, **hint)
     partials = torch.empty(plan["num_clusters"] * plan["partial_stride"], dtype=torch.int32,
                            device=dev)
     bins = torch.empty(num_bins, dtype=torch.int32, device=dev)
@@ -421,18 +430,19 @@ def run_ours(a, world, rank, local):
     prod_steps = max(1, min(a.steps, 500))
     prod_out = torch.empty(num_bins, dtype=torch.int32, device=dev)
     for _ in range(3):
-        pkg.dsmem_hist(keys, num_bins, out=prod_out, stream=stream)
+        pkg.dsmem_hist(keys, num_bins, out=prod_out, stream=stream, **hint)
     torch.cuda.synchronize(dev)
     ev_start.record(stream)
     for _ in range(prod_steps):
-        pkg.dsmem_hist(keys, num_bins, out=prod_out, stream=stream)
+        pkg.dsmem_hist(keys, num_bins, out=prod_out, stream=stream, **hint)
     ev_end.record(stream)
     torch.cuda.synchronize(dev)
     prod_ms = ev_start.elapsed_time(ev_end) / prod_steps
     product_call = {"call": "dsmem_hist (planner, pool scratch alloc + free, cluster kernel, "
                             "reduction)",
-                    "plan": {k: v for k, v in pkg.dsmem_hist_plan(num_bins, n).items()
-                             if k in ("cluster_size", "num_clusters", "kernel", "passes")},
+                    "plan": {k: v for k, v in pkg.dsmem_hist_plan(num_bins, n, **hint).items()
+                             if k in ("cluster_size", "num_clusters", "kernel", "passes",
+                                      "hot_bin")},
                     "ms_per_step": prod_ms, "value": world * n / (prod_ms / 1e3), "unit": UNIT,
                     "steps": prod_steps}
     if parity is not None:

@@ -51,7 +51,7 @@ class Plan(ctypes.Structure):
         ("kernel", ctypes.c_int32),
         ("keys_per_thread", ctypes.c_int32),
         ("sub_vectors", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("hot_bin", ctypes.c_int32),
         ("partial_stride", ctypes.c_int64),
         ("workspace_bytes", ctypes.c_int64),
     ]
@@ -89,6 +89,8 @@ class Request(ctypes.Structure):
         ("aggregate", ctypes.c_int32),
         ("max_slice_bytes", ctypes.c_int32),
         ("kernel", ctypes.c_int32),
+        ("hot_bin_valid", ctypes.c_int32),
+        ("hot_bin", ctypes.c_int32),
     ]
 
 
@@ -173,8 +175,9 @@ def _check(code: int) -> None:
 
 
 def _request(cluster_size=0, block_threads=0, num_clusters=0, aggregate=-1, max_slice_bytes=0,
-             kernel=-1):
-    return Request(cluster_size, block_threads, num_clusters, aggregate, max_slice_bytes, kernel)
+             kernel=-1, hot_bin=-1):
+    return Request(cluster_size, block_threads, num_clusters, aggregate, max_slice_bytes, kernel,
+                   1 if hot_bin >= 0 else 0, max(hot_bin, 0))
 
 
 def _stream_handle(stream):
@@ -205,23 +208,24 @@ def _out_bins(keys, num_bins, out):
 
 
 def dsmem_hist(keys, num_bins: int, out=None, stream=None, *, cluster_size=0, block_threads=0,
-               num_clusters=0, aggregate=-1, max_slice_bytes=0, kernel=-1):
+               num_clusters=0, aggregate=-1, max_slice_bytes=0, kernel=-1, hot_bin=-1):
     """Histogram of a CUDA int32 tensor into `num_bins` 32-bit counters.
 
     Returns a torch.int32 tensor holding the uint32 counts bit for bit (use
     ``.view(torch.uint32)`` or numpy ``.view(np.uint32)`` to read them
     unsigned).  Asynchronous on `stream` (default: torch's current stream).
-    Keyword arguments force parts of the launch shape (0 / -1 = planner).
+    Keyword arguments force parts of the launch shape (0 / -1 = planner);
+    `hot_bin` names a bin expected to take a large share of the keys.
     """
     import torch
     _check_keys(keys, num_bins)
     out = _out_bins(keys, num_bins, out)
     with torch.cuda.device(keys.device):
         forced = (cluster_size, block_threads, num_clusters, max_slice_bytes) != (0, 0, 0, 0) \
-            or aggregate != -1 or kernel != -1
+            or aggregate != -1 or kernel != -1 or hot_bin != -1
         if forced:
             req = _request(cluster_size, block_threads, num_clusters, aggregate, max_slice_bytes,
-                           kernel)
+                           kernel, hot_bin)
             _check(lib().dsmem_hist_ex(keys.data_ptr(), keys.numel(), int(num_bins),
                                        out.data_ptr(), ctypes.byref(req), _stream_handle(stream)))
         else:

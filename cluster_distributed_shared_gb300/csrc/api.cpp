@@ -220,7 +220,7 @@ cudaError_t launch_plan(const dsmem_hist_plan_t& plan, const ClusterHistArgs& ar
 // (more passes) until one fits.  g_mutex must be held.
 int plan_locked(DeviceState* st, int32_t num_bins, int64_t n, const dsmem_hist_request_t* req_in,
                 dsmem_hist_plan_t* out) {
-  dsmem_hist_request_t req = {0, 0, 0, -1, 0, -1};
+  dsmem_hist_request_t req = {0, 0, 0, -1, 0, -1, 0, 0};
   if (req_in) req = *req_in;
   // Environment overrides for sweeps (only where the caller left a field open).
   if (req.cluster_size == 0) req.cluster_size = env_int("DSMEM_HIST_CLUSTER", 0);
@@ -338,6 +338,8 @@ ClusterHistArgs make_args(const dsmem_hist_plan_t& plan, const int32_t* keys, in
   a.status = nullptr;
   a.wait_cycles = wait_cycles_setting();
   a.withhold_last = env_flag("DSMEM_HIST_TEST_WITHHOLD_LAST_ROUND") ? 1u : 0u;
+  a.hot_bin = plan.kernel == DSMEM_HIST_KERNEL_SHIP && plan.hot_bin >= 0
+                  ? static_cast<uint32_t>(plan.hot_bin) : 0xFFFFFFFFu;
   return a;
 }
 
@@ -411,6 +413,9 @@ int check_plan(const DeviceState* st, const dsmem_hist_plan_t* p, int32_t num_bi
     return fail(DSMEM_HIST_EINVAL, "plan: num_clusters / aggregate invalid");
   if (p->partial_stride < num_bins || (p->partial_stride & 3))
     return fail(DSMEM_HIST_EINVAL, "plan: partial_stride must be >= num_bins and a multiple of 4");
+  if (p->hot_bin < -1 || p->hot_bin >= num_bins ||
+      (p->hot_bin >= 0 && p->kernel != DSMEM_HIST_KERNEL_SHIP))
+    return fail(DSMEM_HIST_EINVAL, "plan: hot_bin must be -1 or a bin of a ship-kernel plan");
   return DSMEM_HIST_OK;
 }
 
@@ -582,7 +587,7 @@ int run_with_fixed_scratch(const int32_t* keys, int64_t n, int32_t num_bins, uin
       // it never exceeds the clusters that can be resident or the rows the
       // scratch holds.
       const int32_t auto_clusters = plan.num_clusters;
-      dsmem_hist_request_t req = {0, 0, static_cast<int32_t>(max_rows_bytes / row_bytes), -1, 0, -1};
+      dsmem_hist_request_t req = {0, 0, static_cast<int32_t>(max_rows_bytes / row_bytes), -1, 0, -1, 0, 0};
       if (req.num_clusters >= auto_clusters || req.num_clusters < 1)
         return fail(DSMEM_HIST_EINVAL, "static scratch: %d rows of %lld bytes do not fit below the "
                     "automatic %d clusters", req.num_clusters, static_cast<long long>(row_bytes),
@@ -664,7 +669,7 @@ int run_tune(const int32_t* keys, int64_t n, int32_t num_bins, int64_t sample_ke
   const int sizes[] = {1, 2, 4, 8, 16};
   for (int P : sizes) {
     for (int k = DSMEM_HIST_KERNEL_DIRECT; k <= DSMEM_HIST_KERNEL_SHIP; ++k) {
-      dsmem_hist_request_t req = {P, 0, 0, 0, 0, k};
+      dsmem_hist_request_t req = {P, 0, 0, 0, 0, k, 0, 0};
       dsmem_hist_plan_t plan;
       {
         std::lock_guard<std::mutex> g(g_mutex);

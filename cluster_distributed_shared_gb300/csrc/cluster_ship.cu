@@ -76,7 +76,17 @@ struct Ctx {
   uint32_t lim0;          // end of owner 0's staging block
   uint32_t blk;           // bytes per owner block: 64 * rows
   uint32_t sink;          // 16-bit store target of keys that are not staged
+  uint32_t hot_rel;       // kSkew: in-pass offset of the caller's hot bin (kNoHot: none in this pass)
 };
+
+// kSkew instantiation (the caller named a hot bin, see the plan's hot_bin):
+// keys of the hot bin are counted per thread in the partition instead of
+// being staged, and each warp sends its total to the owner once, at the end
+// of the pass.  One bin holding a quarter of the keys otherwise overflows its
+// owner's staging columns on every round, and every overflowing key costs a
+// remote red (about 0.33 per clock per SM).  The comparison costs about 9%
+// more instructions, so the planner leaves it off unless asked.
+constexpr uint32_t kNoHot = 0xFFFFFFFFu;
 
 // Owner and local counter of an in-pass offset `rel` < P*S.
 __device__ __forceinline__ void owner_local(uint32_t rel, const Ctx& c, uint32_t& o,
@@ -106,8 +116,8 @@ __device__ __forceinline__ void stage_entry(uint32_t ea, uint32_t lim, uint32_t 
 // issued before the first store so their latencies overlap.  kBase0: the
 // pass starts at bin 0, so a key is its own in-pass offset.  kRunTest: test
 // first whether the tile holds one key (off when the caller already has).
-template <bool kPow2, bool kBase0, bool kRunTest>
-__device__ __forceinline__ void partition_tile(const int4& v, const Ctx& c) {
+template <bool kPow2, bool kBase0, bool kRunTest, bool kSkew>
+__device__ __forceinline__ void partition_tile(const int4& v, const Ctx& c, uint32_t& hot_keys) {
   if (kRunTest && __all_sync(kFullMask, v.x == v.w)) {  // rare on most inputs: then test the whole tile
     const int32_t k0 = __shfl_sync(kFullMask, v.x, 0);
     const bool eq4 = (v.x == v.y) & (v.y == v.z) & (v.z == v.w);
@@ -126,9 +136,19 @@ __device__ __forceinline__ void partition_tile(const int4& v, const Ctx& c) {
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     // Offsets at or past P*S clamp to owner P, the always-full cursor row.
-    const uint32_t rel = min(static_cast<uint32_t>(keys[k]) - (kBase0 ? 0u : c.base), c.PS);
-    owner_local(rel, c, own[k], loc[k], kPow2);
-    ea[k] = atom_add_local(c.cur_lane + (own[k] << 7), 64u);
+    if constexpr (kSkew) {
+      const uint32_t rel0 = static_cast<uint32_t>(keys[k]) - (kBase0 ? 0u : c.base);
+      const bool hot = rel0 == c.hot_rel;
+      hot_keys += hot ? 1u : 0u;
+      const uint32_t rel = min(rel0, c.PS);
+      owner_local(rel, c, own[k], loc[k], kPow2);
+      // A hot key reserves nothing; its 16-bit store goes to this lane's sink.
+      ea[k] = hot ? c.sink : atom_add_local(c.cur_lane + (own[k] << 7), 64u);
+    } else {
+      const uint32_t rel = min(static_cast<uint32_t>(keys[k]) - (kBase0 ? 0u : c.base), c.PS);
+      owner_local(rel, c, own[k], loc[k], kPow2);
+      ea[k] = atom_add_local(c.cur_lane + (own[k] << 7), 64u);
+    }
   }
   uint32_t spill = 0;
 #pragma unroll
@@ -144,8 +164,9 @@ __device__ __forceinline__ void partition_tile(const int4& v, const Ctx& c) {
   }
 }
 
-template <int kTiles, bool kPow2>
-__device__ __forceinline__ void partition_round(const int4 (&v)[kTiles], const Ctx& c) {
+template <int kTiles, bool kPow2, bool kSkew>
+__device__ __forceinline__ void partition_round(const int4 (&v)[kTiles], const Ctx& c,
+                                                uint32_t& hot_keys) {
   static_assert(kTiles == 1 || kTiles == 2, "one or two tiles per warp and round");
   // The warp's tiles are consecutive in the input.  The first tile's run test
   // runs here: a run tile followed by a run tile of the same key (a run of
@@ -165,21 +186,21 @@ __device__ __forceinline__ void partition_round(const int4 (&v)[kTiles], const C
       }
       if (kTiles == 1 || both) return;
       if (c.base == 0)
-        partition_tile<kPow2, true, true>(w, c);
+        partition_tile<kPow2, true, true, kSkew>(w, c, hot_keys);
       else
-        partition_tile<kPow2, false, true>(w, c);
+        partition_tile<kPow2, false, true, kSkew>(w, c, hot_keys);
       return;
     }
   }
   // Past here the first tile is known not to be a run.
   if (c.base == 0) {
-    partition_tile<kPow2, true, false>(v[0], c);
+    partition_tile<kPow2, true, false, kSkew>(v[0], c, hot_keys);
 #pragma unroll
-    for (int u = 1; u < kTiles; ++u) partition_tile<kPow2, true, true>(v[u], c);
+    for (int u = 1; u < kTiles; ++u) partition_tile<kPow2, true, true, kSkew>(v[u], c, hot_keys);
   } else {
-    partition_tile<kPow2, false, false>(v[0], c);
+    partition_tile<kPow2, false, false, kSkew>(v[0], c, hot_keys);
 #pragma unroll
-    for (int u = 1; u < kTiles; ++u) partition_tile<kPow2, false, true>(v[u], c);
+    for (int u = 1; u < kTiles; ++u) partition_tile<kPow2, false, true, kSkew>(v[u], c, hot_keys);
   }
 }
 
@@ -239,7 +260,7 @@ __device__ __forceinline__ void load_round(int4 (&v)[kKpt / 4], const int4* vec,
   }
 }
 
-template <int kKpt, bool kPow2>
+template <int kKpt, bool kPow2, bool kSkew>
 __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const ClusterHistArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   Ctx c;
@@ -272,6 +293,7 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
   // A bounded wait of this CTA timed out in this launch (cleared below, before
   // the first cluster barrier, so before any wait).
   const uint32_t gave_up = header0 + 208u;
+  uint32_t hot_keys = 0;  // kSkew: keys of the hot bin this thread counted in this pass
   const uint32_t stage0 = header0 + 256u;
   const uint32_t buf_bytes = P * c.blk;   // one staging or inbox buffer
   const uint32_t inbox0 = stage0 + 2u * buf_bytes;
@@ -323,6 +345,8 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
     c.base = pass * P * c.S;
     const uint32_t left = a.num_bins - c.base;
     c.range = left < P * c.S ? left : P * c.S;
+    c.hot_rel = a.hot_bin - c.base;
+    if (!kSkew || a.hot_bin == kNoHot || c.hot_rel >= c.range) c.hot_rel = kNoHot;
 
     uint4* s4 = reinterpret_cast<uint4*>(smem);
     for (uint32_t i = threadIdx.x; i < (c.S + 32u) / 4; i += blockDim.x) s4[i] = make_uint4(0, 0, 0, 0);
@@ -346,7 +370,7 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
       load_round<kKpt>(cur, vec, ntiles, wtile0, rounds == 1);
       c.cur_lane = cur_lane0;
       c.lim0 = stage0 + c.blk;
-      partition_round<kTiles, kPow2>(cur, c);
+      partition_round<kTiles, kPow2, kSkew>(cur, c, hot_keys);
       if (rounds > 1) load_round<kKpt>(cur, vec, ntiles, wtile0 + per_round, rounds == 2);
     }
     __syncthreads();  // round 0 staged
@@ -402,7 +426,7 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
         // still ship and apply round r; then load round r + 2.
         c.cur_lane = cur_lane0 + k1 * set_bytes;
         c.lim0 = stage0 + (b ^ 1u) * buf_bytes + c.blk;
-        partition_round<kTiles, kPow2>(cur, c);
+        partition_round<kTiles, kPow2, kSkew>(cur, c, hot_keys);
         if (r + 2 < rounds)
           load_round<kKpt>(cur, vec, ntiles, wtile0 + (r + 2) * per_round, r + 3 == rounds);
       }
@@ -433,6 +457,17 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
           red_add_cluster(map_rank(c.slice + 4u * loc, o), 1u);
         }
       }
+    }
+
+    if constexpr (kSkew) {
+      // The hot bin's keys of this pass, one remote increment per warp.
+      const uint32_t t = __reduce_add_sync(kFullMask, hot_keys);
+      if (c.lane == 0 && t != 0u) {
+        uint32_t o, loc;
+        owner_local(c.hot_rel, c, o, loc, kPow2);
+        red_add_cluster(map_rank(c.slice + 4u * loc, o), t);
+      }
+      hot_keys = 0;
     }
 
     cluster_barrier();  // every increment has landed; only own memory after this
@@ -473,14 +508,18 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
   }
 }
 
-template <int kKpt, bool kPow2>
+template <int kKpt, bool kPow2, bool kSkew>
 void* kernel_ptr_t() {
-  return reinterpret_cast<void*>(&cluster_ship_kernel<kKpt, kPow2>);
+  return reinterpret_cast<void*>(&cluster_ship_kernel<kKpt, kPow2, kSkew>);
 }
 
-void* ship_kernel_ptr(int kpt, bool pow2) {
-  if (kpt == 8) return pow2 ? kernel_ptr_t<8, true>() : kernel_ptr_t<8, false>();
-  return pow2 ? kernel_ptr_t<4, true>() : kernel_ptr_t<4, false>();
+void* ship_kernel_ptr(int kpt, bool pow2, bool skew) {
+  if (skew) {
+    if (kpt == 8) return pow2 ? kernel_ptr_t<8, true, true>() : kernel_ptr_t<8, false, true>();
+    return pow2 ? kernel_ptr_t<4, true, true>() : kernel_ptr_t<4, false, true>();
+  }
+  if (kpt == 8) return pow2 ? kernel_ptr_t<8, true, false>() : kernel_ptr_t<8, false, false>();
+  return pow2 ? kernel_ptr_t<4, true, false>() : kernel_ptr_t<4, false, false>();
 }
 
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
@@ -495,8 +534,8 @@ cudaError_t read_and_clear_ship_status(uint32_t* out) {
 }
 
 cudaError_t prepare_ship_kernel(int kpt, int smem_bytes) {
-  for (int p2 = 0; p2 < 2; ++p2) {
-    const void* fn = ship_kernel_ptr(kpt, p2 != 0);
+  for (int v = 0; v < 4; ++v) {
+    const void* fn = ship_kernel_ptr(kpt, (v & 1) != 0, (v & 2) != 0);
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -517,7 +556,7 @@ cudaError_t query_ship_active_clusters(int kpt, int cluster_size, int smem_bytes
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(out, ship_kernel_ptr(kpt, true), &cfg);
+  return cudaOccupancyMaxActiveClusters(out, ship_kernel_ptr(kpt, true, false), &cfg);
 }
 
 // Largest cluster that can be co-scheduled for this kernel with `smem_bytes`
@@ -527,7 +566,7 @@ cudaError_t query_ship_potential_cluster_size(int kpt, int smem_bytes, int* out)
   cfg.gridDim = dim3(16, 1, 1);
   cfg.blockDim = dim3(kShipThreads, 1, 1);
   cfg.dynamicSmemBytes = smem_bytes;
-  return cudaOccupancyMaxPotentialClusterSize(out, ship_kernel_ptr(kpt, true), &cfg);
+  return cudaOccupancyMaxPotentialClusterSize(out, ship_kernel_ptr(kpt, true, false), &cfg);
 }
 
 cudaError_t launch_cluster_ship(const dsmem_hist_plan_t& plan, const ClusterHistArgs& args,
@@ -545,11 +584,18 @@ cudaError_t launch_cluster_ship(const dsmem_hist_plan_t& plan, const ClusterHist
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const bool p2 = is_pow2(plan.bins_per_cta);
+  if (args.hot_bin != kNoHot) {
+    if (plan.keys_per_thread == 8)
+      return p2 ? cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, true, true>, args)
+                : cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, false, true>, args);
+    return p2 ? cudaLaunchKernelEx(&cfg, cluster_ship_kernel<4, true, true>, args)
+              : cudaLaunchKernelEx(&cfg, cluster_ship_kernel<4, false, true>, args);
+  }
   if (plan.keys_per_thread == 8)
-    return p2 ? cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, true>, args)
-              : cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, false>, args);
-  return p2 ? cudaLaunchKernelEx(&cfg, cluster_ship_kernel<4, true>, args)
-            : cudaLaunchKernelEx(&cfg, cluster_ship_kernel<4, false>, args);
+    return p2 ? cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, true, false>, args)
+              : cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, false, false>, args);
+  return p2 ? cudaLaunchKernelEx(&cfg, cluster_ship_kernel<4, true, false>, args)
+            : cudaLaunchKernelEx(&cfg, cluster_ship_kernel<4, false, false>, args);
 }
 
 }  // namespace dsmh

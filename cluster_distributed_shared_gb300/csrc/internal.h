@@ -53,6 +53,7 @@ struct ClusterHistArgs {
   uint32_t* status;
   long long wait_cycles;    // bound of one inbox wait (clock64 cycles)
   uint32_t withhold_last;   // test only: senders skip the last round's arrival and stores
+  uint32_t hot_bin;         // ship kernel: the plan's hot bin, 0xFFFFFFFF for none
 };
 
 // Default bound of one inbox wait: ~1e8 cycles, about 50 ms at 2 GHz.

@@ -18,6 +18,10 @@ uniform-256M-256K      268,435,456    262,144   uniform on [0, 262144)
 zipf1.1-256M-256K      268,435,456    262,144   Zipf(s=1.1) ranks, randomly permuted
 runs256-1G-512K        1,073,741,824  524,288   50% uniform, 50% runs of 256 equal keys
 =====================  =============  ========  =======================================
+
+and one skewed case beside them: hot25-256M-256K, 268,435,456 keys over 262,144
+bins, of which a quarter (each key independently with probability 1/4) are one
+hot bin drawn from the seed and the rest uniform.
 """
 from __future__ import annotations
 
@@ -41,6 +45,7 @@ WORKLOADS = {
     "uniform-256M-256K": dict(n=1 << 28, num_bins=262144, dist="uniform"),
     "zipf1.1-256M-256K": dict(n=1 << 28, num_bins=262144, dist="zipf", s=1.1),
     "runs256-1G-512K": dict(n=1 << 30, num_bins=524288, dist="runs", run_len=256),
+    "hot25-256M-256K": dict(n=1 << 28, num_bins=262144, dist="hot", share=0.25),
 }
 
 
@@ -74,6 +79,10 @@ def _load():
         lib.gen_zipf.restype = ctypes.c_int
         lib.gen_zipf_tables.argtypes = [u32, ctypes.c_double, u64, p, p]
         lib.gen_zipf_tables.restype = ctypes.c_int
+        lib.gen_hot.argtypes = [p, i64, i64, u32, u32, u64]
+        lib.gen_hot.restype = None
+        lib.gen_hot_bin.argtypes = [u32, u64]
+        lib.gen_hot_bin.restype = u32
         _lib = lib
     return _lib
 
@@ -133,6 +142,21 @@ def zipf(n: int, num_bins: int, seed: int, s: float = 1.1,
     return _fill(out, fn, threads)
 
 
+def hot_bin(num_bins: int, seed: int) -> int:
+    """The hot bin of `hot` for this seed."""
+    return int(_load().gen_hot_bin(num_bins, seed & (2**64 - 1)))
+
+
+def hot(n: int, num_bins: int, seed: int, share: float = 0.25, out: np.ndarray | None = None,
+        threads: int | None = None) -> np.ndarray:
+    """Each key is hot_bin(num_bins, seed) with probability `share`, else
+    uniform on [0, num_bins)."""
+    lib = _load()
+    out = np.empty(n, np.int32) if out is None else out
+    thr = min(int(round(share * 2**32)), 2**32 - 1)
+    return _fill(out, lambda p, o, c: lib.gen_hot(p, o, c, num_bins, thr, seed), threads)
+
+
 def zipf_tables(num_bins: int, s: float, seed: int):
     """(cdf over ranks, rank -> bin permutation) exactly as gen_zipf uses them."""
     cdf = np.empty(num_bins, np.float64)
@@ -154,4 +178,6 @@ def workload(name: str, seed: int, out: np.ndarray | None = None,
         return zipf(n, w["num_bins"], seed, w["s"], out, threads)
     if w["dist"] == "runs":
         return runs(n, w["num_bins"], seed, w["run_len"], out, threads)
+    if w["dist"] == "hot":
+        return hot(n, w["num_bins"], seed, w["share"], out, threads)
     raise KeyError(name)

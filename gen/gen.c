@@ -78,6 +78,24 @@ void gen_runs(int32_t* out, int64_t offset, int64_t count, int64_t n,
   }
 }
 
+/* One hot bin plus uniform keys.  The hot bin is draw 0 of the stream
+ * seed ^ GOLDEN_GAMMA mapped to [0, num_bins).  Key i takes the hot bin when
+ * the low 32 bits of draw i of stream `seed` fall below hot_share (a fraction
+ * of 2^32), and otherwise the uniform value of that draw's top bits. */
+uint32_t gen_hot_bin(uint32_t num_bins, uint64_t seed) {
+  return to_range(gen_splitmix64_draw(seed ^ GOLDEN_GAMMA, 0), num_bins, log2_exact(num_bins));
+}
+
+void gen_hot(int32_t* out, int64_t offset, int64_t count, uint32_t num_bins, uint32_t hot_share,
+             uint64_t seed) {
+  int lg = log2_exact(num_bins);
+  uint32_t hot = gen_hot_bin(num_bins, seed);
+  for (int64_t j = 0; j < count; ++j) {
+    uint64_t u = gen_splitmix64_draw(seed, (uint64_t)(offset + j));
+    out[j] = (int32_t)((uint32_t)u < hot_share ? hot : to_range(u, num_bins, lg));
+  }
+}
+
 /* Zipf tables: cdf over ranks, a guide table for O(1) expected search
  * (Chen and Asau's indexed search), and the rank -> bin permutation. */
 typedef struct {

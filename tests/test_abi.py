@@ -277,3 +277,19 @@ def test_ship_threads_match_header():
     m = re.search(r"^#define DSMEM_HIST_SHIP_THREADS (\d+)", header, re.M)
     assert m and int(m.group(1)) == pkg.SHIP_THREADS
     assert pkg.SHIP_THREADS % 32 == 0 and 32 * 17 <= pkg.SHIP_THREADS <= 1024
+
+
+def test_planner_hot_bin_hint():
+    p = plan(GB300, 262144, 1 << 28, 15)
+    assert p["hot_bin"] == -1                      # no hint: the default kernel
+    h = plan(GB300, 262144, 1 << 28, 15, hot_bin=146157)
+    assert h["hot_bin"] == 146157 and h["kernel"] == pkg.KERNEL_SHIP
+    assert {k: v for k, v in h.items() if k != "hot_bin"} == \
+        {k: v for k, v in p.items() if k != "hot_bin"}  # same shape otherwise
+    assert plan(GB300, 262144, 1 << 28, 15, hot_bin=0)["hot_bin"] == 0
+    # the direct kernel ignores the hint
+    assert plan(GB300, 262144, 1 << 28, 15, hot_bin=7, kernel=pkg.KERNEL_DIRECT)["hot_bin"] == -1
+    for bad in (262144, 10 ** 6):
+        with pytest.raises(pkg.DsmemHistError) as e:
+            plan(GB300, 262144, 1 << 28, 15, hot_bin=bad)
+        assert e.value.code == pkg.DSMEM_HIST_EINVAL

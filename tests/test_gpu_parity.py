@@ -393,3 +393,49 @@ def test_environment_overrides_fill_open_request_fields(monkeypatch):
     assert forced["kernel"] == SH and forced["cluster_size"] == 8   # explicit fields win
     keys = gen.uniform(1 << 20, 262144, seed=12)
     assert np.array_equal(gpu_hist(keys, 262144), oracle.histogram(keys, 262144))
+
+
+@pytest.mark.parametrize("share", [0.0, 0.25, 0.6])
+def test_hot_bin_hint_is_exact(share):
+    """The hinted ship kernel (the hot bin's keys counted per thread instead of
+    staged) against the oracle: with and without the hint, a hint on a bin
+    that is not hot, at P = 8 and P = 2, and across passes."""
+    n, num_bins = 1 << 24, 262144
+    keys = gen.hot(n, num_bins, seed=61, share=share)
+    hb = gen.hot_bin(num_bins, 61)
+    keys[:5] = [-1, num_bins, 2 ** 31 - 1, -2 ** 31, hb]   # out-of-range keys ride along
+    keys[1000:1128] = hb                                     # a whole tile of the hot bin
+    want = oracle.histogram(keys, num_bins)
+    d = torch.from_numpy(keys).cuda()
+    for kw in (dict(cluster_size=8), dict(cluster_size=8, hot_bin=hb), dict(cluster_size=8, hot_bin=3),
+               dict(cluster_size=2, hot_bin=hb), dict(cluster_size=16, hot_bin=hb),
+               dict(cluster_size=8, hot_bin=hb, num_clusters=3)):
+        got = to_np(pkg.dsmem_hist(d, num_bins, **kw))
+        torch.cuda.synchronize()
+        assert np.array_equal(got, want), (share, kw, np.flatnonzero(got != want)[:8])
+    plan = pkg.dsmem_hist_plan(num_bins, n, cluster_size=2, hot_bin=hb)
+    assert plan["hot_bin"] == hb and plan["passes"] == 4   # the hot bin lies in one of four passes
+    # through the two-stage entry points with the hinted plan
+    partials = torch.empty(plan["num_clusters"] * plan["partial_stride"], dtype=torch.int32,
+                           device="cuda")
+    pkg.dsmem_hist_partials(d, num_bins, plan, partials)
+    got = to_np(pkg.dsmem_hist_reduce(partials, plan["num_clusters"], plan["partial_stride"],
+                                      num_bins))
+    torch.cuda.synchronize()
+    assert np.array_equal(got, want)
+
+
+def test_hot_workload_full_size_with_and_without_hint():
+    keys, num_bins = _full_workload("hot25-256M-256K", 0)
+    want = oracle.histogram(keys, num_bins)
+    hb = gen.hot_bin(num_bins, 0)
+    assert want.argmax() == hb
+    d = torch.from_numpy(keys).cuda()
+    del keys
+    out = torch.full((num_bins,), -1, dtype=torch.int32, device="cuda")
+    for kw in (dict(cluster_size=8), dict(cluster_size=8, hot_bin=hb)):
+        pkg.dsmem_hist(d, num_bins, out=out, **kw)
+        torch.cuda.synchronize()
+        assert np.array_equal(to_np(out), want), kw
+    del d
+    torch.cuda.empty_cache()

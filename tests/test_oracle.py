@@ -148,3 +148,18 @@ def test_runs_structure():
     assert (tail == tail[:, :1]).all()
     assert keys.min() >= 0 and keys.max() < num_bins
     assert len(np.unique(tail[:, 0])) > 50
+
+
+def test_hot_generator_share_and_bin():
+    n, num_bins = 1 << 20, 262144
+    keys = gen.hot(n, num_bins, seed=5, share=0.25)
+    hb = gen.hot_bin(num_bins, 5)
+    counts = np.bincount(keys, minlength=num_bins)
+    assert counts.argmax() == hb
+    # a quarter of the keys are the hot bin (binomial sd about 0.0004 here),
+    # plus its ordinary uniform share
+    assert abs(counts[hb] / n - (0.25 + 0.75 / num_bins)) < 0.003
+    assert keys.min() >= 0 and keys.max() < num_bins
+    # the same bytes whatever the thread count
+    assert np.array_equal(keys, gen.hot(n, num_bins, seed=5, share=0.25, threads=1))
+    assert np.array_equal(gen.workload("hot25-256M-256K", 5, n=n), keys)
