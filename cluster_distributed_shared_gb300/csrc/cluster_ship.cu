@@ -137,10 +137,12 @@ __device__ __forceinline__ void partition_tile(const int4& v, const Ctx& c, uint
   for (int k = 0; k < 4; ++k) {
     // Offsets at or past P*S clamp to owner P, the always-full cursor row.
     if constexpr (kSkew) {
-      const uint32_t rel0 = static_cast<uint32_t>(keys[k]) - (kBase0 ? 0u : c.base);
-      const bool hot = rel0 == c.hot_rel;
+      // Compare the clamped offset: it is at most P*S, while hot_rel is either
+      // below the pass's range or kNoHot, so no key of a pass without the hot
+      // bin can match (the unclamped offset of key base - 1 equals kNoHot).
+      const uint32_t rel = min(static_cast<uint32_t>(keys[k]) - (kBase0 ? 0u : c.base), c.PS);
+      const bool hot = rel == c.hot_rel;
       hot_keys += hot ? 1u : 0u;
-      const uint32_t rel = min(rel0, c.PS);
       owner_local(rel, c, own[k], loc[k], kPow2);
       // A hot key reserves nothing; its 16-bit store goes to this lane's sink.
       ea[k] = hot ? c.sink : atom_add_local(c.cur_lane + (own[k] << 7), 64u);
@@ -462,7 +464,7 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
     if constexpr (kSkew) {
       // The hot bin's keys of this pass, one remote increment per warp.
       const uint32_t t = __reduce_add_sync(kFullMask, hot_keys);
-      if (c.lane == 0 && t != 0u) {
+      if (c.lane == 0 && t != 0u && c.hot_rel < c.range) {
         uint32_t o, loc;
         owner_local(c.hot_rel, c, o, loc, kPow2);
         red_add_cluster(map_rank(c.slice + 4u * loc, o), t);
