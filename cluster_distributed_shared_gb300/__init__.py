@@ -175,9 +175,11 @@ def _check(code: int) -> None:
 
 
 def _request(cluster_size=0, block_threads=0, num_clusters=0, aggregate=-1, max_slice_bytes=0,
-             kernel=-1, hot_bin=-1):
+             kernel=-1, hot_bin=None):
+    # hot_bin: None = automatic, a bin >= 0 = that hint, -1 = never the hot-bin kernel
+    valid = 0 if hot_bin is None else (1 if hot_bin >= 0 else -1)
     return Request(cluster_size, block_threads, num_clusters, aggregate, max_slice_bytes, kernel,
-                   1 if hot_bin >= 0 else 0, max(hot_bin, 0))
+                   valid, max(hot_bin or 0, 0))
 
 
 def _stream_handle(stream):
@@ -208,21 +210,22 @@ def _out_bins(keys, num_bins, out):
 
 
 def dsmem_hist(keys, num_bins: int, out=None, stream=None, *, cluster_size=0, block_threads=0,
-               num_clusters=0, aggregate=-1, max_slice_bytes=0, kernel=-1, hot_bin=-1):
+               num_clusters=0, aggregate=-1, max_slice_bytes=0, kernel=-1, hot_bin=None):
     """Histogram of a CUDA int32 tensor into `num_bins` 32-bit counters.
 
     Returns a torch.int32 tensor holding the uint32 counts bit for bit (use
     ``.view(torch.uint32)`` or numpy ``.view(np.uint32)`` to read them
     unsigned).  Asynchronous on `stream` (default: torch's current stream).
     Keyword arguments force parts of the launch shape (0 / -1 = planner);
-    `hot_bin` names a bin expected to take a large share of the keys.
+    `hot_bin` names a bin expected to take a large share of the keys (None:
+    automatic, from the previous histogram on the same stream; -1: never).
     """
     import torch
     _check_keys(keys, num_bins)
     out = _out_bins(keys, num_bins, out)
     with torch.cuda.device(keys.device):
         forced = (cluster_size, block_threads, num_clusters, max_slice_bytes) != (0, 0, 0, 0) \
-            or aggregate != -1 or kernel != -1 or hot_bin != -1
+            or aggregate != -1 or kernel != -1 or hot_bin is not None
         if forced:
             req = _request(cluster_size, block_threads, num_clusters, aggregate, max_slice_bytes,
                            kernel, hot_bin)

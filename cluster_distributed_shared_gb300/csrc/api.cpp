@@ -56,16 +56,40 @@ struct DeviceState {
   // (kernel, variant, threads, smem) -> largest co-schedulable cluster size
   std::map<std::tuple<int, int, int, int>, int> potential;
   std::mutex host_call;  // serialises dsmem_hist_host on this device
-  // Per-stream status words of the ship kernel in pinned, host-mapped memory
-  // (h_status on the host, d_status the same words for the device).
+  // Per-stream words in pinned, host-mapped memory (h_status on the host,
+  // d_status the same memory for the device): kStatusSlots u32 status words of
+  // the ship kernel, then one u64 hot-bin word per slot, (seq << 32) | bin as
+  // the reduction of the slot's last histogram wrote it.
   uint32_t* h_status = nullptr;
   uint32_t* d_status = nullptr;
   std::map<cudaStream_t, int> status_slot;
+  // Per slot, host side: the sequence number and bin count of the last
+  // histogram started on it.
+  uint32_t slot_seq[kStatusSlots] = {};
+  int32_t slot_bins[kStatusSlots] = {};
 };
 
-// Status words per device: one per stream, up to this many streams; later
-// streams share the last word.
-constexpr int kStatusSlots = 64;
+// Bytes of the host-mapped block: status words, then hot-bin words.
+constexpr size_t kMappedBytes = kStatusSlots * (sizeof(uint32_t) + sizeof(unsigned long long));
+// The hot-bin kernel is chosen when one bin held at least 1/kHotShareDen of
+// the keys of the previous histogram on the same stream.
+constexpr int64_t kHotShareDen = 6;
+
+// One stream's words; all null when the device has none (see stream_slot).
+struct SlotRef {
+  int slot = -1;
+  uint32_t* h_status = nullptr;
+  uint32_t* d_status = nullptr;
+  unsigned long long* h_hot = nullptr;
+  unsigned long long* d_hot = nullptr;
+};
+
+// What the reduction of a histogram reports for the next call on its stream.
+struct HotReport {
+  uint32_t min_count = 0;  // 0: nothing
+  unsigned long long* word = nullptr;
+  uint32_t seq = 0;
+};
 
 std::mutex g_mutex;
 std::map<int, DeviceState*> g_devices;
@@ -127,18 +151,16 @@ bool env_flag(const char* name) {
 }
 bool injected_alloc_failure() { return env_flag("DSMEM_HIST_TEST_FAIL_ALLOC"); }
 
-// This stream's status word (host and device views); g_mutex must be held.
-// With may_alloc false, a device whose status words were never allocated
-// gets none (both null).
-int status_word(DeviceState* st, cudaStream_t stream, bool may_alloc, uint32_t** h, uint32_t** d) {
-  *h = *d = nullptr;
+// This stream's words (host and device views); g_mutex must be held.  With
+// may_alloc false, a device whose words were never allocated gets none.
+int stream_slot(DeviceState* st, cudaStream_t stream, bool may_alloc, SlotRef* r) {
+  *r = SlotRef{};
   if (!st->h_status) {
     if (!may_alloc) return DSMEM_HIST_OK;
     void* p = nullptr;
-    cudaError_t e = cudaHostAlloc(&p, kStatusSlots * sizeof(uint32_t),
-                                  cudaHostAllocMapped | cudaHostAllocPortable);
+    cudaError_t e = cudaHostAlloc(&p, kMappedBytes, cudaHostAllocMapped | cudaHostAllocPortable);
     if (e != cudaSuccess) return fail_cuda(e, "cudaHostAlloc (status words)");
-    memset(p, 0, kStatusSlots * sizeof(uint32_t));
+    memset(p, 0, kMappedBytes);
     void* dp = nullptr;
     if ((e = cudaHostGetDevicePointer(&dp, p, 0)) != cudaSuccess) {
       cudaFreeHost(p);
@@ -155,9 +177,46 @@ int status_word(DeviceState* st, cudaStream_t stream, bool may_alloc, uint32_t**
     slot = std::min<int>(static_cast<int>(st->status_slot.size()), kStatusSlots - 1);
     st->status_slot[stream] = slot;
   }
-  *h = st->h_status + slot;
-  *d = st->d_status + slot;
+  r->slot = slot;
+  r->h_status = st->h_status + slot;
+  r->d_status = st->d_status + slot;
+  r->h_hot = reinterpret_cast<unsigned long long*>(st->h_status + kStatusSlots) + slot;
+  r->d_hot = reinterpret_cast<unsigned long long*>(st->d_status + kStatusSlots) + slot;
   return DSMEM_HIST_OK;
+}
+
+// The hot bin for a histogram of n keys into num_bins bins on this stream
+// slot, or -1.  It is the bin the reduction of the previous histogram started
+// on the slot reported as holding at least 1/kHotShareDen of its keys, if that
+// histogram had the same bin count and its report has landed (its sequence
+// number matches).  Also sets up *report for this call's reduction.  g_mutex
+// must be held.
+int32_t choose_hot_bin(DeviceState* st, const SlotRef& r, int64_t n, int32_t num_bins,
+                       HotReport* report) {
+  *report = HotReport{};
+  if (r.slot < 0 || !r.h_hot) return -1;
+  const unsigned long long w = *reinterpret_cast<volatile unsigned long long*>(r.h_hot);
+  const uint32_t prev_seq = st->slot_seq[r.slot];
+  const int32_t prev_bins = st->slot_bins[r.slot];
+  int32_t hot = -1;
+  if (prev_seq != 0 && prev_bins == num_bins && static_cast<uint32_t>(w >> 32) == prev_seq &&
+      static_cast<uint32_t>(w) < static_cast<uint32_t>(num_bins)) {
+    hot = static_cast<int32_t>(static_cast<uint32_t>(w));
+    if (trace_enabled())
+      fprintf(stderr, "[dsmem_hist] stream slot %d: bin %d held a sixth or more of the keys of "
+              "the last histogram -> hot-bin kernel\n", r.slot, hot);
+  }
+  uint32_t seq = prev_seq + 1;
+  if (seq == 0) seq = 1;
+  st->slot_seq[r.slot] = seq;
+  st->slot_bins[r.slot] = num_bins;
+  const int64_t min_count = (n + kHotShareDen - 1) / kHotShareDen;
+  if (n > 0 && min_count <= 0xFFFFFFFFll) {
+    report->min_count = static_cast<uint32_t>(min_count);
+    report->word = r.d_hot;
+    report->seq = seq;
+  }
+  return hot;
 }
 
 // Reports (once) a bounded wait that gave up in an earlier launch on this
@@ -349,14 +408,20 @@ int run_device(const int32_t* keys, int64_t n, int32_t num_bins, uint32_t* bins,
   if (rc) return rc;
   dsmem_hist_plan_t plan;
   DeviceState* st = nullptr;
-  uint32_t *h_status = nullptr, *d_status = nullptr;
+  SlotRef sr;
+  HotReport hot_report;
   {
     std::lock_guard<std::mutex> g(g_mutex);
     if ((rc = device_state(&st))) return rc;
-    if ((rc = status_word(st, stream, true, &h_status, &d_status))) return rc;
-    if ((rc = take_pending_timeout(h_status))) return rc;
+    if ((rc = stream_slot(st, stream, true, &sr))) return rc;
+    if ((rc = take_pending_timeout(sr.h_status))) return rc;
     if ((rc = plan_locked(st, num_bins, n, req, &plan))) return rc;
     if ((rc = ensure_pool(st))) return rc;
+    // The hot-bin kernel: on the caller's request, or (unless the caller
+    // turned it off) when the previous histogram on this stream had a hot bin.
+    const int32_t chosen = choose_hot_bin(st, sr, n, num_bins, &hot_report);
+    if ((!req || req->hot_bin_valid == 0) && plan.kernel == DSMEM_HIST_KERNEL_SHIP)
+      plan.hot_bin = chosen;
   }
   cudaError_t e;
   if (n == 0) {
@@ -375,11 +440,12 @@ int run_device(const int32_t* keys, int64_t n, int32_t num_bins, uint32_t* bins,
   }
   uint32_t* partials = static_cast<uint32_t*>(scratch);
   ClusterHistArgs args = make_args(plan, keys, n, num_bins, partials, 0);
-  args.status = d_status;
+  args.status = sr.d_status;
   e = launch_plan(plan, args, stream);
   if (e == cudaSuccess)
     e = launch_reduce_partials(partials, args.stride, static_cast<uint32_t>(plan.num_clusters),
-                               args.num_bins, bins, stream);
+                               args.num_bins, bins, stream, hot_report.min_count,
+                               hot_report.word, hot_report.seq);
   const cudaError_t ef = cudaFreeAsync(scratch, stream);
   if (e != cudaSuccess) return fail_cuda(e, "cluster histogram launch");
   if (ef != cudaSuccess) return fail_cuda(ef, "cudaFreeAsync");
@@ -426,7 +492,7 @@ int run_partials(const int32_t* keys, int64_t n, int32_t num_bins, const dsmem_h
   if (reinterpret_cast<uintptr_t>(partials) & 15u)
     return fail(DSMEM_HIST_EINVAL, "partials must be 16-byte aligned");
   if (accumulate != 0 && accumulate != 1) return fail(DSMEM_HIST_EINVAL, "accumulate must be 0 or 1");
-  uint32_t *h_status = nullptr, *d_status = nullptr;
+  SlotRef sr;
   {
     std::lock_guard<std::mutex> g(g_mutex);
     DeviceState* st = nullptr;
@@ -434,12 +500,13 @@ int run_partials(const int32_t* keys, int64_t n, int32_t num_bins, const dsmem_h
     if ((rc = check_plan(st, plan, num_bins))) return rc;
     if (plan->kernel == DSMEM_HIST_KERNEL_SHIP && n >= kShipMaxKeys)
       return fail(DSMEM_HIST_EINVAL, "the ship kernel takes fewer than 2^38 keys per call");
-    if ((rc = status_word(st, stream, true, &h_status, &d_status))) return rc;
-    if ((rc = take_pending_timeout(h_status))) return rc;
+    if ((rc = stream_slot(st, stream, true, &sr))) return rc;
+    if ((rc = take_pending_timeout(sr.h_status))) return rc;
     if ((rc = prepare_locked(st, *plan))) return rc;
   }
+  // The caller's plan decides the kernel (its hot_bin included): no automatic choice.
   ClusterHistArgs args = make_args(*plan, keys, n, num_bins, partials, accumulate);
-  args.status = d_status;
+  args.status = sr.d_status;
   const cudaError_t e = launch_plan(*plan, args, stream);
   return e == cudaSuccess ? DSMEM_HIST_OK : fail_cuda(e, "cluster histogram launch");
 }
@@ -468,14 +535,17 @@ int run_host(const int32_t* h_keys, int64_t n, int32_t num_bins, uint32_t* h_bin
   DeviceState* st = nullptr;
   dsmem_hist_plan_t plan;
   const int64_t chunk = n < kHostChunkKeys ? n : kHostChunkKeys;
-  uint32_t *h_status = nullptr, *d_status = nullptr;
+  SlotRef sr;
+  HotReport hot_report;
   {
     std::lock_guard<std::mutex> g(g_mutex);
     if ((rc = device_state(&st))) return rc;
-    if ((rc = status_word(st, stream, true, &h_status, &d_status))) return rc;
-    if ((rc = take_pending_timeout(h_status))) return rc;
+    if ((rc = stream_slot(st, stream, true, &sr))) return rc;
+    if ((rc = take_pending_timeout(sr.h_status))) return rc;
     if ((rc = plan_locked(st, num_bins, chunk, nullptr, &plan))) return rc;
     if ((rc = ensure_pool(st))) return rc;
+    const int32_t chosen = choose_hot_bin(st, sr, n, num_bins, &hot_report);
+    if (plan.kernel == DSMEM_HIST_KERNEL_SHIP) plan.hot_bin = chosen;
     cudaError_t e;
     if (!st->copy_stream) {
       if ((e = cudaStreamCreateWithFlags(&st->copy_stream, cudaStreamNonBlocking)) != cudaSuccess)
@@ -529,7 +599,7 @@ int run_host(const int32_t* h_keys, int64_t n, int32_t num_bins, uint32_t* h_bin
       break;
     }
     ClusterHistArgs args = make_args(plan, stage[b], cnt, num_bins, partials, j > 0);
-    args.status = d_status;
+    args.status = sr.d_status;
     if ((e = launch_plan(plan, args, stream)) != cudaSuccess ||
         (e = cudaEventRecord(st->ev_consumed[b], stream)) != cudaSuccess) {
       rc = fail_cuda(e, "cluster histogram launch");
@@ -539,7 +609,9 @@ int run_host(const int32_t* h_keys, int64_t n, int32_t num_bins, uint32_t* h_bin
   if (rc == DSMEM_HIST_OK && n > 0) {
     if ((e = launch_reduce_partials(partials, static_cast<uint64_t>(plan.partial_stride),
                                     static_cast<uint32_t>(plan.num_clusters),
-                                    static_cast<uint32_t>(num_bins), d_bins, stream)) != cudaSuccess)
+                                    static_cast<uint32_t>(num_bins), d_bins, stream,
+                                    hot_report.min_count, hot_report.word,
+                                    hot_report.seq)) != cudaSuccess)
       rc = fail_cuda(e, "reduce launch");
   }
   if (rc == DSMEM_HIST_OK) {
@@ -571,15 +643,16 @@ int run_with_fixed_scratch(const int32_t* keys, int64_t n, int32_t num_bins, uin
                 num_bins, static_cast<long long>(row_bytes), static_cast<long long>(max_rows_bytes),
                 static_cast<long long>(max_rows_bytes / 4));
   dsmem_hist_plan_t plan;
-  uint32_t *h_status = nullptr, *d_status = nullptr;
+  SlotRef sr;
+  HotReport hot_report;
   {
     std::lock_guard<std::mutex> g(g_mutex);
     DeviceState* st = nullptr;
     if ((rc = device_state(&st))) return rc;
-    // Status words only if an earlier call already allocated them: this path
+    // Stream words only if an earlier call already allocated them: this path
     // allocates nothing.
-    if ((rc = status_word(st, stream, false, &h_status, &d_status))) return rc;
-    if ((rc = take_pending_timeout(h_status))) return rc;
+    if ((rc = stream_slot(st, stream, false, &sr))) return rc;
+    if ((rc = take_pending_timeout(sr.h_status))) return rc;
     if ((rc = plan_locked(st, num_bins, n, nullptr, &plan))) return rc;
     if (plan.workspace_bytes > max_rows_bytes) {
       // Fewer clusters, so their partial rows fit the static scratch.  The
@@ -596,6 +669,8 @@ int run_with_fixed_scratch(const int32_t* keys, int64_t n, int32_t num_bins, uin
       if (plan.num_clusters > req.num_clusters || plan.workspace_bytes > max_rows_bytes)
         return fail(DSMEM_HIST_EINVAL, "static scratch: forced plan exceeds the scratch");
     }
+    const int32_t chosen = choose_hot_bin(st, sr, n, num_bins, &hot_report);
+    if (plan.kernel == DSMEM_HIST_KERNEL_SHIP) plan.hot_bin = chosen;
   }
   cudaError_t e;
   if (n == 0) {
@@ -603,11 +678,12 @@ int run_with_fixed_scratch(const int32_t* keys, int64_t n, int32_t num_bins, uin
     return e == cudaSuccess ? DSMEM_HIST_OK : fail_cuda(e, "cudaMemsetAsync");
   }
   ClusterHistArgs args = make_args(plan, keys, n, num_bins, scratch, 0);
-  args.status = d_status;
+  args.status = sr.d_status;
   e = launch_plan(plan, args, stream);
   if (e == cudaSuccess)
     e = launch_reduce_partials(scratch, args.stride, static_cast<uint32_t>(plan.num_clusters),
-                               args.num_bins, bins, stream);
+                               args.num_bins, bins, stream, hot_report.min_count,
+                               hot_report.word, hot_report.seq);
   return e == cudaSuccess ? DSMEM_HIST_OK : fail_cuda(e, "cluster histogram launch");
 }
 
@@ -842,6 +918,7 @@ void dsmem_hist_release(void) {
       cudaFreeHost(st->h_status);
       st->h_status = st->d_status = nullptr;
       st->status_slot.clear();
+      for (int i = 0; i < kStatusSlots; ++i) st->slot_seq[i] = 0, st->slot_bins[i] = 0;
     }
     if (st->copy_stream) {
       cudaStreamDestroy(st->copy_stream);

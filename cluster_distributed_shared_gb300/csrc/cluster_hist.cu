@@ -173,12 +173,19 @@ __global__ void __launch_bounds__(1024, 1) cluster_hist_kernel(const ClusterHist
 // partial row of those columns with four loads in flight, so a thread waits
 // on about ceil(C / 4G) loads in turn instead of ceil(C / 4), and the groups'
 // sums meet in shared memory.
+// With hot_word non-null the kernel also reports hot bins: a thread whose bin
+// holds at least hot_min keys writes (seq << 32) | bin to *hot_word (pinned,
+// host-mapped).  At most n / hot_min bins can qualify, and the library takes
+// any one of them to pick the hot-bin kernel for the next call on the same
+// stream; the sequence number tells it which call the word belongs to.
 template <int G>
 __global__ void __launch_bounds__(256) reduce_partials_kernel(const uint32_t* __restrict__ partials,
                                                               uint64_t stride, uint32_t num_clusters,
                                                               uint32_t num_bins,
                                                               uint32_t* __restrict__ bins,
-                                                              int bins_vec_ok) {
+                                                              int bins_vec_ok, uint32_t hot_min,
+                                                              unsigned long long* hot_word,
+                                                              uint32_t seq) {
   constexpr uint32_t kCols = 256 / G;
   __shared__ uint4 part[G][kCols];
   const uint32_t col = threadIdx.x % kCols, g = threadIdx.x / kCols;
@@ -232,6 +239,15 @@ __global__ void __launch_bounds__(256) reduce_partials_kernel(const uint32_t* __
         if (b + 1 < num_bins) bins[b + 1] = s.y;
         if (b + 2 < num_bins) bins[b + 2] = s.z;
         if (b + 3 < num_bins) bins[b + 3] = s.w;
+      }
+      if (hot_word) {
+        // Bins past num_bins are row padding (always zero) and never qualify.
+        const uint32_t c4[4] = {s.x, s.y, s.z, s.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (c4[q] >= hot_min && b + q < num_bins)
+            *reinterpret_cast<volatile unsigned long long*>(hot_word) =
+                (static_cast<unsigned long long>(seq) << 32) | (b + q);
       }
     }
   }
@@ -365,7 +381,9 @@ cudaError_t launch_cluster_hist(const dsmem_hist_plan_t& plan, const ClusterHist
 
 cudaError_t launch_reduce_partials(const uint32_t* partials, uint64_t stride,
                                    uint32_t num_clusters, uint32_t num_bins, uint32_t* bins,
-                                   cudaStream_t stream) {
+                                   cudaStream_t stream, uint32_t hot_min,
+                                   unsigned long long* hot_word, uint32_t seq) {
+  if (hot_min == 0) hot_word = nullptr;
   const uint32_t nv = (num_bins + 3) / 4;
   const int vec_ok = (reinterpret_cast<uintptr_t>(bins) & 15u) == 0;
   // Row groups: the largest power of two <= min(16, C).
@@ -375,19 +393,19 @@ cudaError_t launch_reduce_partials(const uint32_t* partials, uint64_t stride,
   if (blocks > 8192) blocks = 8192;
   switch (G) {
     case 16:
-      reduce_partials_kernel<16><<<blocks, 256, 0, stream>>>(partials, stride, num_clusters, num_bins, bins, vec_ok);
+      reduce_partials_kernel<16><<<blocks, 256, 0, stream>>>(partials, stride, num_clusters, num_bins, bins, vec_ok, hot_min, hot_word, seq);
       break;
     case 8:
-      reduce_partials_kernel<8><<<blocks, 256, 0, stream>>>(partials, stride, num_clusters, num_bins, bins, vec_ok);
+      reduce_partials_kernel<8><<<blocks, 256, 0, stream>>>(partials, stride, num_clusters, num_bins, bins, vec_ok, hot_min, hot_word, seq);
       break;
     case 4:
-      reduce_partials_kernel<4><<<blocks, 256, 0, stream>>>(partials, stride, num_clusters, num_bins, bins, vec_ok);
+      reduce_partials_kernel<4><<<blocks, 256, 0, stream>>>(partials, stride, num_clusters, num_bins, bins, vec_ok, hot_min, hot_word, seq);
       break;
     case 2:
-      reduce_partials_kernel<2><<<blocks, 256, 0, stream>>>(partials, stride, num_clusters, num_bins, bins, vec_ok);
+      reduce_partials_kernel<2><<<blocks, 256, 0, stream>>>(partials, stride, num_clusters, num_bins, bins, vec_ok, hot_min, hot_word, seq);
       break;
     default:
-      reduce_partials_kernel<1><<<blocks, 256, 0, stream>>>(partials, stride, num_clusters, num_bins, bins, vec_ok);
+      reduce_partials_kernel<1><<<blocks, 256, 0, stream>>>(partials, stride, num_clusters, num_bins, bins, vec_ok, hot_min, hot_word, seq);
   }
   return cudaGetLastError();
 }

@@ -208,7 +208,7 @@ int plan_shape(const dsmem_hist_device_t* dev, int32_t num_bins, int64_t n,
   out->ctas_per_sm = per_sm;
   out->max_active_clusters = max_active_clusters > 0 ? max_active_clusters : 0;
   out->hot_bin = -1;
-  if (req->hot_bin_valid && kernel == DSMEM_HIST_KERNEL_SHIP) {
+  if (req->hot_bin_valid > 0 && kernel == DSMEM_HIST_KERNEL_SHIP) {
     if (req->hot_bin < 0 || req->hot_bin >= num_bins) {
       *why = "hot_bin must lie in [0, num_bins)";
       return DSMEM_HIST_EINVAL;

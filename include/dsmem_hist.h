@@ -108,9 +108,10 @@ typedef struct dsmem_hist_plan {
   int32_t keys_per_thread;     /* ship kernel: keys each thread partitions per round (4 or 8) */
   int32_t sub_vectors;         /* ship kernel: rows of each owner's staging block (each row:
                                   32 columns of 16-bit entries) */
-  int32_t hot_bin;             /* ship kernel: a bin the caller expects to hold a large share of
-                                  the keys; its keys are counted in registers instead of staged
-                                  (see dsmem_hist_request_t.hot_bin).  -1: none, the default */
+  int32_t hot_bin;             /* ship kernel: a bin expected to hold a large share of the keys;
+                                  its keys are counted in registers instead of staged (see
+                                  dsmem_hist_request_t.hot_bin).  -1: none.  The planner sets it
+                                  only on request; dsmem_hist_partials uses it as given */
   int64_t partial_stride;      /* u32 elements between two clusters' partial rows (num_bins rounded up to 4) */
   int64_t workspace_bytes;     /* scratch: num_clusters * partial_stride * 4 */
 } dsmem_hist_plan_t;
@@ -123,14 +124,22 @@ typedef struct dsmem_hist_request {
   int32_t aggregate;       /* -1 choose, 0 off, 1 on */
   int32_t max_slice_bytes; /* cap on 4*S (default 128 KiB) */
   int32_t kernel;          /* -1 choose, else DSMEM_HIST_KERNEL_* */
-  int32_t hot_bin_valid;   /* nonzero: hot_bin below is a hint */
-  int32_t hot_bin;         /* a bin in [0, num_bins) expected to take a large share of the keys
-                              (a tenth or more).  The ship kernel then counts that bin's keys in
-                              registers instead of staging them; one bin with a quarter of the
-                              keys otherwise overflows its owner's staging columns every round and
-                              sends each overflowing key as a remote atomic.  The comparison costs
-                              about 9% more instructions on keys without such a bin.  Exact either
-                              way; ignored by the direct kernel. */
+  int32_t hot_bin_valid;   /* 0: automatic (see below); 1: hot_bin below is a hint; -1: never
+                              use the hot-bin kernel */
+  int32_t hot_bin;         /* with hot_bin_valid == 1: a bin in [0, num_bins) expected to take a
+                              large share of the keys (a sixth or more).  The ship kernel then
+                              counts that bin's keys in registers instead of staging them; one
+                              bin with a quarter of the keys otherwise overflows its owner's
+                              staging columns every round and sends each overflowing key as a
+                              remote atomic.  The comparison costs about 9% more instructions on
+                              keys without such a bin.  Exact either way; ignored by the direct
+                              kernel.
+                              Automatic: dsmem_hist, dsmem_hist_ex (hot_bin_valid == 0),
+                              dsmem_hist_host and dsmem_hist_static use the hot-bin kernel when
+                              the previous histogram on the same stream had the same num_bins
+                              and one bin held a sixth or more of its keys, as that histogram's
+                              reduction reported it (without a device synchronisation: a report
+                              that has not landed yet counts as none). */
 } dsmem_hist_request_t;
 
 /* The device facts the planner uses; filled from cudaGetDeviceProperties by

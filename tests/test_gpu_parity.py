@@ -439,3 +439,62 @@ def test_hot_workload_full_size_with_and_without_hint():
         assert np.array_equal(to_np(out), want), kw
     del d
     torch.cuda.empty_cache()
+
+
+_AUTO_SCRIPT = r"""
+import sys, numpy as np, torch
+sys.path.insert(0, sys.argv[1])
+import cluster_distributed_shared_gb300 as pkg, gen, oracle
+n, nb = 1 << 24, 262144
+hot = gen.hot(n, nb, seed=81, share=0.25)
+uni = gen.uniform(n, nb, seed=82)
+s = torch.cuda.Stream()
+for tag, keys in [("hot1", hot), ("hot2", hot), ("hot3", hot), ("uni1", uni), ("uni2", uni),
+                  ("hot4", hot), ("hot5", hot)]:
+    d = torch.from_numpy(keys).cuda()
+    torch.cuda.synchronize()
+    print("CALL", tag, file=sys.stderr, flush=True)
+    got = pkg.dsmem_hist(d, nb, stream=s)      # automatic choice
+    s.synchronize()
+    ok = np.array_equal(got.cpu().numpy().view(np.uint32), oracle.histogram(keys, nb))
+    print("PARITY", tag, ok, file=sys.stderr, flush=True)
+# the caller can turn the choice off
+d = torch.from_numpy(hot).cuda()
+print("CALL off", file=sys.stderr, flush=True)
+got = pkg.dsmem_hist(d, nb, stream=s, hot_bin=-1)
+s.synchronize()
+print("PARITY off", np.array_equal(got.cpu().numpy().view(np.uint32), oracle.histogram(hot, nb)),
+      file=sys.stderr, flush=True)
+print("HOTBIN", gen.hot_bin(nb, 81), file=sys.stderr, flush=True)
+"""
+
+
+def test_hot_bin_kernel_is_chosen_from_the_previous_histogram():
+    """A bin with a quarter of the keys makes the next call on the same stream
+    take the hot-bin kernel; uniform keys switch it off again; every call is
+    exact."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, DSMEM_HIST_TRACE="1")
+    out = subprocess.run([sys.executable, "-c", _AUTO_SCRIPT, root], env=env, capture_output=True,
+                         text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-3000:]
+    lines = out.stderr.splitlines()
+    hot_bin = int([l for l in lines if l.startswith("HOTBIN")][0].split()[1])
+    chose, current = {}, None
+    for l in lines:
+        if l.startswith("CALL"):
+            current = l.split()[1]
+            chose[current] = None
+        elif "-> hot-bin kernel" in l and current is not None:
+            chose[current] = int(l.split("bin ")[1].split()[0])
+        elif l.startswith("PARITY"):
+            assert l.split()[2] == "True", l
+    assert chose["hot1"] is None                        # nothing known yet
+    assert chose["hot2"] == chose["hot3"] == hot_bin    # the previous call had the hot bin
+    assert chose["uni1"] == hot_bin                     # chosen from the hot call before it
+    assert chose["uni2"] is None                        # uniform keys report no hot bin
+    assert chose["hot4"] is None and chose["hot5"] == hot_bin
+    assert chose["off"] is None
