@@ -192,6 +192,18 @@ int stream_slot(DeviceState* st, cudaStream_t stream, bool may_alloc, SlotRef* r
 // number matches).  Also sets up *report for this call's reduction.  g_mutex
 // must be held.
 int32_t choose_hot_bin(DeviceState* st, const SlotRef& r, int64_t n, int32_t num_bins,
+                       HotReport* report);
+
+// Takes the automatic choice into a ship-kernel plan (tracing it).
+void use_hot_bin(dsmem_hist_plan_t* plan, int32_t chosen, const SlotRef& r) {
+  if (chosen < 0 || plan->kernel != DSMEM_HIST_KERNEL_SHIP) return;
+  plan->hot_bin = chosen;
+  if (trace_enabled())
+    fprintf(stderr, "[dsmem_hist] stream slot %d: bin %d held a sixth or more of the keys of the "
+            "last histogram -> hot-bin kernel\n", r.slot, chosen);
+}
+
+int32_t choose_hot_bin(DeviceState* st, const SlotRef& r, int64_t n, int32_t num_bins,
                        HotReport* report) {
   *report = HotReport{};
   if (r.slot < 0 || !r.h_hot) return -1;
@@ -202,9 +214,6 @@ int32_t choose_hot_bin(DeviceState* st, const SlotRef& r, int64_t n, int32_t num
   if (prev_seq != 0 && prev_bins == num_bins && static_cast<uint32_t>(w >> 32) == prev_seq &&
       static_cast<uint32_t>(w) < static_cast<uint32_t>(num_bins)) {
     hot = static_cast<int32_t>(static_cast<uint32_t>(w));
-    if (trace_enabled())
-      fprintf(stderr, "[dsmem_hist] stream slot %d: bin %d held a sixth or more of the keys of "
-              "the last histogram -> hot-bin kernel\n", r.slot, hot);
   }
   uint32_t seq = prev_seq + 1;
   if (seq == 0) seq = 1;
@@ -420,8 +429,7 @@ int run_device(const int32_t* keys, int64_t n, int32_t num_bins, uint32_t* bins,
     // The hot-bin kernel: on the caller's request, or (unless the caller
     // turned it off) when the previous histogram on this stream had a hot bin.
     const int32_t chosen = choose_hot_bin(st, sr, n, num_bins, &hot_report);
-    if ((!req || req->hot_bin_valid == 0) && plan.kernel == DSMEM_HIST_KERNEL_SHIP)
-      plan.hot_bin = chosen;
+    if (!req || req->hot_bin_valid == 0) use_hot_bin(&plan, chosen, sr);
   }
   cudaError_t e;
   if (n == 0) {
@@ -545,7 +553,7 @@ int run_host(const int32_t* h_keys, int64_t n, int32_t num_bins, uint32_t* h_bin
     if ((rc = plan_locked(st, num_bins, chunk, nullptr, &plan))) return rc;
     if ((rc = ensure_pool(st))) return rc;
     const int32_t chosen = choose_hot_bin(st, sr, n, num_bins, &hot_report);
-    if (plan.kernel == DSMEM_HIST_KERNEL_SHIP) plan.hot_bin = chosen;
+    use_hot_bin(&plan, chosen, sr);
     cudaError_t e;
     if (!st->copy_stream) {
       if ((e = cudaStreamCreateWithFlags(&st->copy_stream, cudaStreamNonBlocking)) != cudaSuccess)
@@ -670,7 +678,7 @@ int run_with_fixed_scratch(const int32_t* keys, int64_t n, int32_t num_bins, uin
         return fail(DSMEM_HIST_EINVAL, "static scratch: forced plan exceeds the scratch");
     }
     const int32_t chosen = choose_hot_bin(st, sr, n, num_bins, &hot_report);
-    if (plan.kernel == DSMEM_HIST_KERNEL_SHIP) plan.hot_bin = chosen;
+    use_hot_bin(&plan, chosen, sr);
   }
   cudaError_t e;
   if (n == 0) {
