@@ -40,6 +40,9 @@ int fail_cuda(cudaError_t e, const char* what) {
   return fail(DSMEM_HIST_ECUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
 }
 
+// Histograms per stream slot whose bin counts the host remembers.
+constexpr uint32_t kSeqHistory = 64;
+
 struct DeviceState {
   bool ready = false;
   dsmem_hist_device_t dev = {};
@@ -57,20 +60,23 @@ struct DeviceState {
   std::map<std::tuple<int, int, int, int>, int> potential;
   std::mutex host_call;  // serialises dsmem_hist_host on this device
   // Per-stream words in pinned, host-mapped memory (h_status on the host,
-  // d_status the same memory for the device): kStatusSlots u32 status words of
-  // the ship kernel, then one u64 hot-bin word per slot, (seq << 32) | bin as
-  // the reduction of the slot's last histogram wrote it.
+  // d_status the same memory for the device), kStatusSlots of each kind: the
+  // ship kernel's u32 status words; u32 sequence stamps, the number of the
+  // latest histogram whose reduction has run on the slot; and u64 hot-bin
+  // words, (seq << 32) | bin for a bin that held a sixth or more of the keys
+  // of histogram seq.
   uint32_t* h_status = nullptr;
   uint32_t* d_status = nullptr;
   std::map<cudaStream_t, int> status_slot;
-  // Per slot, host side: the sequence number and bin count of the last
-  // histogram started on it.
+  // Per slot, host side: the last sequence number handed out, and the bin
+  // counts of the last kSeqHistory histograms by sequence number.
   uint32_t slot_seq[kStatusSlots] = {};
-  int32_t slot_bins[kStatusSlots] = {};
+  uint32_t hist_seq[kStatusSlots][kSeqHistory] = {};
+  int32_t hist_bins[kStatusSlots][kSeqHistory] = {};
 };
 
-// Bytes of the host-mapped block: status words, then hot-bin words.
-constexpr size_t kMappedBytes = kStatusSlots * (sizeof(uint32_t) + sizeof(unsigned long long));
+// Bytes of the host-mapped block: status words, sequence stamps, hot-bin words.
+constexpr size_t kMappedBytes = kStatusSlots * (2 * sizeof(uint32_t) + sizeof(unsigned long long));
 // The hot-bin kernel is chosen when one bin held at least 1/kHotShareDen of
 // the keys of the previous histogram on the same stream.
 constexpr int64_t kHotShareDen = 6;
@@ -80,14 +86,17 @@ struct SlotRef {
   int slot = -1;
   uint32_t* h_status = nullptr;
   uint32_t* d_status = nullptr;
+  uint32_t* h_seq = nullptr;
+  uint32_t* d_seq = nullptr;
   unsigned long long* h_hot = nullptr;
   unsigned long long* d_hot = nullptr;
 };
 
-// What the reduction of a histogram reports for the next call on its stream.
+// What the reduction of a histogram reports for later calls on its stream.
 struct HotReport {
   uint32_t min_count = 0;  // 0: nothing
   unsigned long long* word = nullptr;
+  uint32_t* seq_word = nullptr;
   uint32_t seq = 0;
 };
 
@@ -180,52 +189,53 @@ int stream_slot(DeviceState* st, cudaStream_t stream, bool may_alloc, SlotRef* r
   r->slot = slot;
   r->h_status = st->h_status + slot;
   r->d_status = st->d_status + slot;
-  r->h_hot = reinterpret_cast<unsigned long long*>(st->h_status + kStatusSlots) + slot;
-  r->d_hot = reinterpret_cast<unsigned long long*>(st->d_status + kStatusSlots) + slot;
+  r->h_seq = st->h_status + kStatusSlots + slot;
+  r->d_seq = st->d_status + kStatusSlots + slot;
+  r->h_hot = reinterpret_cast<unsigned long long*>(st->h_status + 2 * kStatusSlots) + slot;
+  r->d_hot = reinterpret_cast<unsigned long long*>(st->d_status + 2 * kStatusSlots) + slot;
   return DSMEM_HIST_OK;
 }
 
 // The hot bin for a histogram of n keys into num_bins bins on this stream
-// slot, or -1.  It is the bin the reduction of the previous histogram started
-// on the slot reported as holding at least 1/kHotShareDen of its keys, if that
-// histogram had the same bin count and its report has landed (its sequence
-// number matches).  Also sets up *report for this call's reduction.  g_mutex
-// must be held.
+// slot, or -1.  It comes from the latest histogram whose reduction has run on
+// the slot (its sequence stamp): if that histogram had the same bin count, the
+// bin it reported as holding a sixth or more of its keys.  Reports arrive
+// asynchronously, so in a loop of calls this is one a few calls back; one
+// with no hot bin switches the choice off again.  Also sets up *report for
+// this call's reduction.  g_mutex must be held.
 int32_t choose_hot_bin(DeviceState* st, const SlotRef& r, int64_t n, int32_t num_bins,
-                       HotReport* report);
+                       HotReport* report) {
+  *report = HotReport{};
+  if (r.slot < 0 || !r.h_hot) return -1;
+  const uint32_t done = *reinterpret_cast<volatile uint32_t*>(r.h_seq);
+  const unsigned long long w = *reinterpret_cast<volatile unsigned long long*>(r.h_hot);
+  const uint32_t k = done % kSeqHistory;
+  int32_t hot = -1;
+  if (done != 0 && st->hist_seq[r.slot][k] == done && st->hist_bins[r.slot][k] == num_bins &&
+      static_cast<uint32_t>(w >> 32) == done && static_cast<uint32_t>(w) < static_cast<uint32_t>(num_bins))
+    hot = static_cast<int32_t>(static_cast<uint32_t>(w));
+  uint32_t seq = st->slot_seq[r.slot] + 1;
+  if (seq == 0) seq = 1;
+  st->slot_seq[r.slot] = seq;
+  st->hist_seq[r.slot][seq % kSeqHistory] = seq;
+  st->hist_bins[r.slot][seq % kSeqHistory] = num_bins;
+  const int64_t min_count = (n + kHotShareDen - 1) / kHotShareDen;
+  if (n > 0 && min_count <= 0xFFFFFFFFll) {
+    report->min_count = static_cast<uint32_t>(min_count);
+    report->word = r.d_hot;
+    report->seq_word = r.d_seq;
+    report->seq = seq;
+  }
+  return hot;
+}
 
 // Takes the automatic choice into a ship-kernel plan (tracing it).
 void use_hot_bin(dsmem_hist_plan_t* plan, int32_t chosen, const SlotRef& r) {
   if (chosen < 0 || plan->kernel != DSMEM_HIST_KERNEL_SHIP) return;
   plan->hot_bin = chosen;
   if (trace_enabled())
-    fprintf(stderr, "[dsmem_hist] stream slot %d: bin %d held a sixth or more of the keys of the "
-            "last histogram -> hot-bin kernel\n", r.slot, chosen);
-}
-
-int32_t choose_hot_bin(DeviceState* st, const SlotRef& r, int64_t n, int32_t num_bins,
-                       HotReport* report) {
-  *report = HotReport{};
-  if (r.slot < 0 || !r.h_hot) return -1;
-  const unsigned long long w = *reinterpret_cast<volatile unsigned long long*>(r.h_hot);
-  const uint32_t prev_seq = st->slot_seq[r.slot];
-  const int32_t prev_bins = st->slot_bins[r.slot];
-  int32_t hot = -1;
-  if (prev_seq != 0 && prev_bins == num_bins && static_cast<uint32_t>(w >> 32) == prev_seq &&
-      static_cast<uint32_t>(w) < static_cast<uint32_t>(num_bins)) {
-    hot = static_cast<int32_t>(static_cast<uint32_t>(w));
-  }
-  uint32_t seq = prev_seq + 1;
-  if (seq == 0) seq = 1;
-  st->slot_seq[r.slot] = seq;
-  st->slot_bins[r.slot] = num_bins;
-  const int64_t min_count = (n + kHotShareDen - 1) / kHotShareDen;
-  if (n > 0 && min_count <= 0xFFFFFFFFll) {
-    report->min_count = static_cast<uint32_t>(min_count);
-    report->word = r.d_hot;
-    report->seq = seq;
-  }
-  return hot;
+    fprintf(stderr, "[dsmem_hist] stream slot %d: bin %d held a sixth or more of the keys of a "
+            "recent histogram -> hot-bin kernel\n", r.slot, chosen);
 }
 
 // Reports (once) a bounded wait that gave up in an earlier launch on this
@@ -453,7 +463,7 @@ int run_device(const int32_t* keys, int64_t n, int32_t num_bins, uint32_t* bins,
   if (e == cudaSuccess)
     e = launch_reduce_partials(partials, args.stride, static_cast<uint32_t>(plan.num_clusters),
                                args.num_bins, bins, stream, hot_report.min_count,
-                               hot_report.word, hot_report.seq);
+                               hot_report.word, hot_report.seq_word, hot_report.seq);
   const cudaError_t ef = cudaFreeAsync(scratch, stream);
   if (e != cudaSuccess) return fail_cuda(e, "cluster histogram launch");
   if (ef != cudaSuccess) return fail_cuda(ef, "cudaFreeAsync");
@@ -619,7 +629,7 @@ int run_host(const int32_t* h_keys, int64_t n, int32_t num_bins, uint32_t* h_bin
                                     static_cast<uint32_t>(plan.num_clusters),
                                     static_cast<uint32_t>(num_bins), d_bins, stream,
                                     hot_report.min_count, hot_report.word,
-                                    hot_report.seq)) != cudaSuccess)
+                                    hot_report.seq_word, hot_report.seq)) != cudaSuccess)
       rc = fail_cuda(e, "reduce launch");
   }
   if (rc == DSMEM_HIST_OK) {
@@ -691,7 +701,7 @@ int run_with_fixed_scratch(const int32_t* keys, int64_t n, int32_t num_bins, uin
   if (e == cudaSuccess)
     e = launch_reduce_partials(scratch, args.stride, static_cast<uint32_t>(plan.num_clusters),
                                args.num_bins, bins, stream, hot_report.min_count,
-                               hot_report.word, hot_report.seq);
+                               hot_report.word, hot_report.seq_word, hot_report.seq);
   return e == cudaSuccess ? DSMEM_HIST_OK : fail_cuda(e, "cluster histogram launch");
 }
 
@@ -926,7 +936,10 @@ void dsmem_hist_release(void) {
       cudaFreeHost(st->h_status);
       st->h_status = st->d_status = nullptr;
       st->status_slot.clear();
-      for (int i = 0; i < kStatusSlots; ++i) st->slot_seq[i] = 0, st->slot_bins[i] = 0;
+      for (int i = 0; i < kStatusSlots; ++i) {
+        st->slot_seq[i] = 0;
+        for (uint32_t j = 0; j < kSeqHistory; ++j) st->hist_seq[i][j] = 0, st->hist_bins[i][j] = 0;
+      }
     }
     if (st->copy_stream) {
       cudaStreamDestroy(st->copy_stream);

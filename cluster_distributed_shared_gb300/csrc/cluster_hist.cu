@@ -173,11 +173,12 @@ __global__ void __launch_bounds__(1024, 1) cluster_hist_kernel(const ClusterHist
 // partial row of those columns with four loads in flight, so a thread waits
 // on about ceil(C / 4G) loads in turn instead of ceil(C / 4), and the groups'
 // sums meet in shared memory.
-// With hot_word non-null the kernel also reports hot bins: a thread whose bin
-// holds at least hot_min keys writes (seq << 32) | bin to *hot_word (pinned,
-// host-mapped).  At most n / hot_min bins can qualify, and the library takes
-// any one of them to pick the hot-bin kernel for the next call on the same
-// stream; the sequence number tells it which call the word belongs to.
+// With hot_word non-null the kernel also reports hot bins, for the library to
+// pick the hot-bin kernel on later calls on the same stream (both words are
+// pinned, host-mapped):
+//   - the first thread stamps *seq_word with this call's sequence number;
+//   - a thread whose bin holds at least hot_min keys writes (seq << 32) | bin
+//     to *hot_word.  At most n / hot_min bins can qualify; any one will do.
 template <int G>
 __global__ void __launch_bounds__(256) reduce_partials_kernel(const uint32_t* __restrict__ partials,
                                                               uint64_t stride, uint32_t num_clusters,
@@ -185,7 +186,8 @@ __global__ void __launch_bounds__(256) reduce_partials_kernel(const uint32_t* __
                                                               uint32_t* __restrict__ bins,
                                                               int bins_vec_ok, uint32_t hot_min,
                                                               unsigned long long* hot_word,
-                                                              uint32_t seq) {
+                                                              uint32_t* seq_word, uint32_t seq) {
+  if (hot_word && blockIdx.x == 0 && threadIdx.x == 0) *reinterpret_cast<volatile uint32_t*>(seq_word) = seq;
   constexpr uint32_t kCols = 256 / G;
   __shared__ uint4 part[G][kCols];
   const uint32_t col = threadIdx.x % kCols, g = threadIdx.x / kCols;
@@ -382,8 +384,8 @@ cudaError_t launch_cluster_hist(const dsmem_hist_plan_t& plan, const ClusterHist
 cudaError_t launch_reduce_partials(const uint32_t* partials, uint64_t stride,
                                    uint32_t num_clusters, uint32_t num_bins, uint32_t* bins,
                                    cudaStream_t stream, uint32_t hot_min,
-                                   unsigned long long* hot_word, uint32_t seq) {
-  if (hot_min == 0) hot_word = nullptr;
+                                   unsigned long long* hot_word, uint32_t* seq_word, uint32_t seq) {
+  if (hot_min == 0 || !seq_word) hot_word = nullptr;
   const uint32_t nv = (num_bins + 3) / 4;
   const int vec_ok = (reinterpret_cast<uintptr_t>(bins) & 15u) == 0;
   // Row groups: the largest power of two <= min(16, C).
@@ -393,19 +395,19 @@ cudaError_t launch_reduce_partials(const uint32_t* partials, uint64_t stride,
   if (blocks > 8192) blocks = 8192;
   switch (G) {
     case 16:
-      reduce_partials_kernel<16><<<blocks, 256, 0, stream>>>(partials, stride, num_clusters, num_bins, bins, vec_ok, hot_min, hot_word, seq);
+      reduce_partials_kernel<16><<<blocks, 256, 0, stream>>>(partials, stride, num_clusters, num_bins, bins, vec_ok, hot_min, hot_word, seq_word, seq);
       break;
     case 8:
-      reduce_partials_kernel<8><<<blocks, 256, 0, stream>>>(partials, stride, num_clusters, num_bins, bins, vec_ok, hot_min, hot_word, seq);
+      reduce_partials_kernel<8><<<blocks, 256, 0, stream>>>(partials, stride, num_clusters, num_bins, bins, vec_ok, hot_min, hot_word, seq_word, seq);
       break;
     case 4:
-      reduce_partials_kernel<4><<<blocks, 256, 0, stream>>>(partials, stride, num_clusters, num_bins, bins, vec_ok, hot_min, hot_word, seq);
+      reduce_partials_kernel<4><<<blocks, 256, 0, stream>>>(partials, stride, num_clusters, num_bins, bins, vec_ok, hot_min, hot_word, seq_word, seq);
       break;
     case 2:
-      reduce_partials_kernel<2><<<blocks, 256, 0, stream>>>(partials, stride, num_clusters, num_bins, bins, vec_ok, hot_min, hot_word, seq);
+      reduce_partials_kernel<2><<<blocks, 256, 0, stream>>>(partials, stride, num_clusters, num_bins, bins, vec_ok, hot_min, hot_word, seq_word, seq);
       break;
     default:
-      reduce_partials_kernel<1><<<blocks, 256, 0, stream>>>(partials, stride, num_clusters, num_bins, bins, vec_ok, hot_min, hot_word, seq);
+      reduce_partials_kernel<1><<<blocks, 256, 0, stream>>>(partials, stride, num_clusters, num_bins, bins, vec_ok, hot_min, hot_word, seq_word, seq);
   }
   return cudaGetLastError();
 }

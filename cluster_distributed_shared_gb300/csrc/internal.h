@@ -66,13 +66,14 @@ constexpr long long kDefaultWaitCycles = 100000000ll;
 // Launches (all asynchronous on `stream`).
 cudaError_t launch_cluster_hist(const dsmem_hist_plan_t& plan, const ClusterHistArgs& args,
                                 cudaStream_t stream);
-// With hot_word non-null and hot_min > 0 the reduction also writes
-// (seq << 32) | bin to *hot_word (pinned, host-mapped) for a bin holding at
-// least hot_min keys, if any does.
+// With hot_word and seq_word non-null and hot_min > 0 the reduction also
+// stamps *seq_word with seq and writes (seq << 32) | bin to *hot_word (both
+// pinned, host-mapped) for a bin holding at least hot_min keys, if any does.
 cudaError_t launch_reduce_partials(const uint32_t* partials, uint64_t stride,
                                    uint32_t num_clusters, uint32_t num_bins, uint32_t* bins,
                                    cudaStream_t stream, uint32_t hot_min = 0,
-                                   unsigned long long* hot_word = nullptr, uint32_t seq = 0);
+                                   unsigned long long* hot_word = nullptr,
+                                   uint32_t* seq_word = nullptr, uint32_t seq = 0);
 cudaError_t launch_global_atomic(const int32_t* keys, int64_t n, uint32_t num_bins,
                                  uint32_t* bins, cudaStream_t stream);
 // Work-free control kernel with a plan's grid, cluster and shared memory.

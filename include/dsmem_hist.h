@@ -136,10 +136,13 @@ typedef struct dsmem_hist_request {
                               kernel.
                               Automatic: dsmem_hist, dsmem_hist_ex (hot_bin_valid == 0),
                               dsmem_hist_host and dsmem_hist_static use the hot-bin kernel when
-                              the previous histogram on the same stream had the same num_bins
-                              and one bin held a sixth or more of its keys, as that histogram's
-                              reduction reported it (without a device synchronisation: a report
-                              that has not landed yet counts as none). */
+                              the latest histogram on the same stream whose reduction has run
+                              had the same num_bins and one bin holding a sixth or more of its
+                              keys, as that reduction reported it through pinned, host-mapped
+                              memory (no device synchronisation).  In a loop of calls that is a
+                              histogram a few calls back; one without such a bin turns the
+                              choice off again.  dsmem_hist_static takes part only on streams
+                              whose words an allocating call has set up. */
 } dsmem_hist_request_t;
 
 /* The device facts the planner uses; filled from cudaGetDeviceProperties by
