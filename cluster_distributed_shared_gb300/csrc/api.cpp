@@ -40,9 +40,6 @@ int fail_cuda(cudaError_t e, const char* what) {
   return fail(DSMEM_HIST_ECUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
 }
 
-// Histograms per stream slot whose bin counts the host remembers.
-constexpr uint32_t kSeqHistory = 64;
-
 struct DeviceState {
   bool ready = false;
   dsmem_hist_device_t dev = {};
@@ -68,11 +65,12 @@ struct DeviceState {
   uint32_t* h_status = nullptr;
   uint32_t* d_status = nullptr;
   std::map<cudaStream_t, int> status_slot;
-  // Per slot, host side: the last sequence number handed out, and the bin
-  // counts of the last kSeqHistory histograms by sequence number.
+  // Per slot, host side: the last sequence number handed out, the bin count
+  // of the latest histogram, and the first sequence number that had it (every
+  // histogram from that one on had the same bin count).
   uint32_t slot_seq[kStatusSlots] = {};
-  uint32_t hist_seq[kStatusSlots][kSeqHistory] = {};
-  int32_t hist_bins[kStatusSlots][kSeqHistory] = {};
+  int32_t slot_bins[kStatusSlots] = {};
+  uint32_t slot_bins_since[kStatusSlots] = {};
 };
 
 // Bytes of the host-mapped block: status words, sequence stamps, hot-bin words.
@@ -198,8 +196,8 @@ int stream_slot(DeviceState* st, cudaStream_t stream, bool may_alloc, SlotRef* r
 
 // The hot bin for a histogram of n keys into num_bins bins on this stream
 // slot, or -1.  It comes from the latest histogram whose reduction has run on
-// the slot (its sequence stamp): if that histogram had the same bin count, the
-// bin it reported as holding a sixth or more of its keys.  Reports arrive
+// the slot (its sequence stamp): if every histogram since had the same bin
+// count, the bin it reported as holding a sixth or more of its keys.  Reports arrive
 // asynchronously, so in a loop of calls this is one a few calls back; one
 // with no hot bin switches the choice off again.  Also sets up *report for
 // this call's reduction.  g_mutex must be held.
@@ -209,16 +207,20 @@ int32_t choose_hot_bin(DeviceState* st, const SlotRef& r, int64_t n, int32_t num
   if (r.slot < 0 || !r.h_hot) return -1;
   const uint32_t done = *reinterpret_cast<volatile uint32_t*>(r.h_seq);
   const unsigned long long w = *reinterpret_cast<volatile unsigned long long*>(r.h_hot);
-  const uint32_t k = done % kSeqHistory;
   int32_t hot = -1;
-  if (done != 0 && st->hist_seq[r.slot][k] == done && st->hist_bins[r.slot][k] == num_bins &&
+  if (done != 0 && st->slot_bins[r.slot] == num_bins && done >= st->slot_bins_since[r.slot] &&
       static_cast<uint32_t>(w >> 32) == done && static_cast<uint32_t>(w) < static_cast<uint32_t>(num_bins))
     hot = static_cast<int32_t>(static_cast<uint32_t>(w));
   uint32_t seq = st->slot_seq[r.slot] + 1;
-  if (seq == 0) seq = 1;
+  if (seq == 0) {  // after 2^32 calls: start over
+    seq = 1;
+    st->slot_bins[r.slot] = 0;
+  }
   st->slot_seq[r.slot] = seq;
-  st->hist_seq[r.slot][seq % kSeqHistory] = seq;
-  st->hist_bins[r.slot][seq % kSeqHistory] = num_bins;
+  if (st->slot_bins[r.slot] != num_bins) {
+    st->slot_bins[r.slot] = num_bins;
+    st->slot_bins_since[r.slot] = seq;
+  }
   const int64_t min_count = (n + kHotShareDen - 1) / kHotShareDen;
   if (n > 0 && min_count <= 0xFFFFFFFFll) {
     report->min_count = static_cast<uint32_t>(min_count);
@@ -936,10 +938,8 @@ void dsmem_hist_release(void) {
       cudaFreeHost(st->h_status);
       st->h_status = st->d_status = nullptr;
       st->status_slot.clear();
-      for (int i = 0; i < kStatusSlots; ++i) {
-        st->slot_seq[i] = 0;
-        for (uint32_t j = 0; j < kSeqHistory; ++j) st->hist_seq[i][j] = 0, st->hist_bins[i][j] = 0;
-      }
+      for (int i = 0; i < kStatusSlots; ++i)
+        st->slot_seq[i] = st->slot_bins_since[i] = 0, st->slot_bins[i] = 0;
     }
     if (st->copy_stream) {
       cudaStreamDestroy(st->copy_stream);
