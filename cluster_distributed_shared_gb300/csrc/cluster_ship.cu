@@ -38,17 +38,19 @@
 //   Apply.  Warps wait (bounded) for a round's mbarrier phase, then apply
 //     that round's inbox block from sender w mod P: one `dp2a` turns a
 //     16-bit entry into its counter's address, one local red increments it.
-// In round r every warp applies round r-1, resets the cursor set of round
-// r+2, arrives on the cluster barrier, ships round r, partitions round r+1
-// into the other staging buffer and loads the keys of round r+2, then waits
-// on the cluster barrier and meets the other warps at the round's only CTA
-// barrier.  Warps that finish applying and shipping partition while others
-// still apply, so the phases overlap.  Since the mbarriers publish the inbox
-// data, the cluster barrier is relaxed: it only tells senders that the inbox
-// they are about to overwrite has been read, so no warp waits for its remote
-// stores to be acknowledged.  A sender writes round r into inbox buffer r%2
-// only after the barrier of round r-1, which every owner arrives on only
-// after it has applied round r-2 from that buffer.
+// In round r every warp applies round r-1, waits (bounded) on the CTA's
+// `staged` mbarrier until every warp has partitioned round r, resets the
+// cursor set of round r+2, arrives on the cluster barrier, ships round r,
+// partitions round r+1 into the other staging buffer, loads the keys of round
+// r+2, arrives on `staged`, and waits on the cluster barrier.  No CTA barrier
+// ends the round: a warp that has partitioned goes on to apply the next
+// round while others still partition, and it only waits for them where it
+// reads what they staged.  Since the mbarriers publish the inbox data, the
+// cluster barrier is relaxed: it only tells senders that the inbox they are
+// about to overwrite has been read, so no warp waits for its remote stores to
+// be acknowledged.  A sender writes round r into inbox buffer r%2 only after
+// the barrier of round r-1, which every owner arrives on only after it has
+// applied round r-2 from that buffer.
 
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -221,13 +223,14 @@ __device__ __forceinline__ void apply_vector(uint32_t slice, const uint4& x) {
 
 __device__ uint32_t g_ship_status;  // bit 0: a bounded wait gave up (until read and cleared)
 
-// Waits for phase `parity` of an inbox mbarrier, at most `limit` cycles
-// (by default ~1e8, about 50 ms).  On a timeout the device status word and
-// the call's host-mapped word (if any) record it, this CTA's shared flag at
-// `gave_up` is set, and the caller skips the buffer; once a wait of this CTA
-// has timed out, its later waits in the same launch give up after one probe.
-// Later launches start with the flag clear.
-__device__ __forceinline__ bool wait_inbox(uint32_t mbar, uint32_t parity, uint32_t gave_up,
+// Waits for phase `parity` of an mbarrier (an inbox buffer's, or the CTA's
+// `staged` one), at most `limit` cycles (by default ~1e8, about 50 ms).  On a
+// timeout the device status word and the call's host-mapped word (if any)
+// record it, this CTA's shared flag at `gave_up` is set, and the caller skips
+// the inbox buffer (or goes on without the other warps); once a wait of this
+// CTA has timed out, its later waits in the same launch give up after one
+// probe.  Later launches start with the flag clear.
+__device__ __forceinline__ bool wait_mbar(uint32_t mbar, uint32_t parity, uint32_t gave_up,
                                            long long limit, uint32_t* status) {
   if (mbar_try_wait(mbar, parity)) return true;
   if (ld_shared_u32(gave_up) != 0u) return false;
@@ -281,7 +284,8 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
 
   // Layout (must match ship_staging_bytes): slice u32[S + 32], cursors
   // u32[3][P + 1][32], headers u32[2][16], sink u16[32], two inbox
-  // mbarriers and a timeout flag (256 bytes with padding), staging u16[2][P][qs][32], inboxes
+  // mbarriers, a timeout flag and the `staged` mbarrier (256 bytes with
+  // padding), staging u16[2][P][qs][32], inboxes
   // u16[2][P][qs][32].  Round r partitions into staging buffer r % 2 with
   // cursor set r % 3, and its blocks travel in inbox buffer r % 2.
   const uint32_t sbase = smem_u32(smem);
@@ -295,6 +299,7 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
   // A bounded wait of this CTA timed out in this launch (cleared below, before
   // the first cluster barrier, so before any wait).
   const uint32_t gave_up = header0 + 208u;
+  const uint32_t staged = header0 + 216u;  // mbarrier: every warp partitioned the next round
   uint32_t hot_keys = 0;  // kSkew: keys of the hot bin this thread counted in this pass
   const uint32_t stage0 = header0 + 256u;
   const uint32_t buf_bytes = P * c.blk;   // one staging or inbox buffer
@@ -363,6 +368,7 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
       // One arrival per other sender and round; their bytes complete it.
       mbar_init(full0, P - 1u);
       mbar_init(full0 + 8u, P - 1u);
+      mbar_init(staged, kWarps);
       fence_mbar_init();
     }
     cluster_barrier();  // slices zeroed and mbarriers initialised cluster-wide
@@ -384,20 +390,26 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
         // arrived and every byte has landed (this CTA's own block was
         // applied straight from staging when it was shipped).
         const uint32_t pb = b ^ 1u;
-        if (wait_inbox(full0 + 8u * pb, ((r - 1u) >> 1) & 1u, gave_up, a.wait_cycles, a.status)) {
+        if (wait_mbar(full0 + 8u * pb, ((r - 1u) >> 1) & 1u, gave_up, a.wait_cycles, a.status)) {
           const uint32_t src = src0 + pb * buf_bytes;
           const uint32_t end = src - vofs + 64u * min(ld_shared_u32(hdr_in + 64u * pb), qs);
           for (uint32_t at = src; at < end; at += step) apply_vector(c.slice, ld_shared_v4(at));
         }
       }
-      // Set (r + 2) % 3 was last read by round r - 1's ship; round r + 2
-      // partitions with it into buffer b.
-      const uint32_t k2 = k == 0 ? 2u : k - 1u;
-      if (resets) st_shared_u32(rs_addr + k2 * set_bytes, b ? rs_val1 : rs_val0);
+      // Round r is staged once every warp has arrived after partitioning it
+      // (in round r - 1, after its ship of round r - 1).  On a timeout the
+      // warp goes on: the launch is already reported, and every access below
+      // stays inside its buffers whatever the cursors hold.
+      if (r > 0) wait_mbar(staged, (r - 1u) & 1u, gave_up, a.wait_cycles, a.status);
       // Relaxed: inbox data is published through the mbarriers; this
       // barrier only tells senders that round r-1's inbox has been read
       // (every load of it has returned: its values fed the reds above).
       cluster_arrive_relaxed();
+      // Set (r + 2) % 3 was last read by round r - 1's ship, which every warp
+      // finished before the wait above; round r + 2 partitions with it into
+      // buffer b, after the wait of round r + 1.
+      const uint32_t k2 = k == 0 ? 2u : k - 1u;
+      if (resets) st_shared_u32(rs_addr + k2 * set_bytes, b ? rs_val1 : rs_val0);
       {
         // Ship owner so's block of round r: rows = its fullest column.
         const uint32_t top = top0 + b * buf_bytes;
@@ -431,14 +443,15 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
         partition_round<kTiles, kPow2, kSkew>(cur, c, hot_keys);
         if (r + 2 < rounds)
           load_round<kKpt>(cur, vec, ntiles, wtile0 + (r + 2) * per_round, r + 3 == rounds);
+        __syncwarp();  // the warp's staging stores and cursor updates precede the arrival
+        if (c.lane == 0) mbar_arrive_local(staged);
       }
       cluster_wait();   // round r's inboxes complete everywhere
-      __syncthreads();  // round r + 1 staged; round r's staging and cursors read
       k = k1;
     }
     if (rounds > 0 && so != rank) {
       const uint32_t pb = (rounds - 1u) & 1u;
-      if (wait_inbox(full0 + 8u * pb, ((rounds - 1u) >> 1) & 1u, gave_up, a.wait_cycles, a.status)) {
+      if (wait_mbar(full0 + 8u * pb, ((rounds - 1u) >> 1) & 1u, gave_up, a.wait_cycles, a.status)) {
         const uint32_t src = src0 + pb * buf_bytes;
         const uint32_t end = src - vofs + 64u * min(ld_shared_u32(hdr_in + 64u * pb), qs);
         for (uint32_t at = src; at < end; at += step) apply_vector(c.slice, ld_shared_v4(at));
@@ -487,6 +500,7 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
     if (threadIdx.x == 0) {
       mbar_inval(full0);
       mbar_inval(full0 + 8u);
+      mbar_inval(staged);
     }
 
     const uint32_t first = c.base + rank * c.S;

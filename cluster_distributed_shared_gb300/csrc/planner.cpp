@@ -35,9 +35,9 @@ uint64_t owner_magic(uint32_t S) { return ((uint64_t{1} << 40) / S) + 1; }
 
 // Shared memory the ship kernel needs beside the slice; the kernel lays it
 // out in this order: 32 padding counters after the slice, three cursor sets
-// u32[P + 1][32], inbox headers u32[2][16] plus a 16-bit sink per lane and
-// two mbarriers (256 bytes), then two staging buffers and two inbox buffers
-// of P blocks of `rows` rows of 64 bytes.
+// u32[P + 1][32], inbox headers u32[2][16] plus a 16-bit sink per lane,
+// three mbarriers and a flag (256 bytes), then two staging buffers and two
+// inbox buffers of P blocks of `rows` rows of 64 bytes.
 uint32_t ship_staging_bytes(int cluster_size, int rows) {
   const uint32_t P = static_cast<uint32_t>(cluster_size), q = static_cast<uint32_t>(rows);
   return 4u * 32u + 3u * 4u * 32u * (P + 1u) + 256u + 4u * P * 64u * q;

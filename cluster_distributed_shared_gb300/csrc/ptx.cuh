@@ -57,6 +57,10 @@ __device__ __forceinline__ void mbar_inval(uint32_t addr) {
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
+// Arrives once on an mbarrier of this CTA (release at CTA scope).
+__device__ __forceinline__ void mbar_arrive_local(uint32_t addr) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(addr) : "memory");
+}
 // Arrives on an mbarrier of a CTA of the cluster (shared::cluster address)
 // and adds `bytes` to its pending transaction count.
 __device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t cluster_addr, uint32_t bytes) {
