@@ -216,10 +216,11 @@ def kernel_sources_sha256(kernel_id):
     return h.hexdigest()
 
 
-def kernel_traffic(n_keys, num_bins, cluster_size, kernel_id, block_threads):
+def kernel_traffic(workload, n_keys, num_bins, cluster_size, kernel_id, block_threads):
     """Per-launch DRAM bytes of the cluster kernel from the committed ncu
-    summary, scaled to this launch's keys; None when the kernel's sources or
-    its block size have changed since the counters were taken."""
+    summary of the same workload, scaled to this launch's keys; None when no
+    capture of that workload and shape exists or the kernel's sources or its
+    block size have changed since the counters were taken."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
@@ -232,8 +233,8 @@ def kernel_traffic(n_keys, num_bins, cluster_size, kernel_id, block_threads):
     if rec.get("kernel_sources_sha256") != sha:
         return None
     for e in rec.get("captures", []):
-        if (e.get("num_bins") == num_bins and e.get("cluster_size") == cluster_size
-                and e.get("block_threads") == block_threads):
+        if (e.get("workload") == workload and e.get("num_bins") == num_bins
+                and e.get("cluster_size") == cluster_size and e.get("block_threads") == block_threads):
             return e["dram_bytes"] * (n_keys / e["n"])
     return None
 
@@ -488,7 +489,7 @@ def run_ours(a, world, rank, local):
     peak, peak_src = hbm_peak()
     alg_bytes = 4 * n + 4 * num_bins
     achieved = alg_bytes / (cluster_ms / 1e3) / 1e9
-    traffic = kernel_traffic(n, num_bins, P, plan["kernel"], plan["block_threads"])
+    traffic = kernel_traffic(cfg["workload"], n, num_bins, P, plan["kernel"], plan["block_threads"])
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
