@@ -326,6 +326,32 @@ def test_repeat_is_deterministic_across_shapes():
             assert np.array_equal(to_np(got), want), kw
 
 
+@pytest.mark.parametrize("P", [2, 4, 8, 16])
+@pytest.mark.parametrize("kpt", [8, 4])
+def test_long_round_chains_in_one_cluster(P, kpt):
+    # One cluster of the ship kernel walks hundreds of rounds, so every
+    # buffer, cursor set and mbarrier phase is reused many times; Zipf keys
+    # make the owners' loads uneven from round to round, and the length
+    # leaves a ragged tail.
+    num_bins = P * 32768
+    n = (1 << 23) + 12345
+    keys_np = gen.zipf(n, num_bins, seed=40 + P)
+    want = oracle.histogram(keys_np, num_bins)
+    keys = torch.from_numpy(keys_np).cuda()
+    plan = pkg.dsmem_hist_plan(num_bins, n, cluster_size=P, kernel=SH, num_clusters=1)
+    plan["keys_per_thread"] = kpt
+    rounds = n // (P * pkg.SHIP_THREADS * kpt)
+    assert plan["num_clusters"] == 1 and plan["bins_per_cta"] == 32768 and rounds >= 70
+    partials = torch.empty(plan["partial_stride"], dtype=torch.int32, device="cuda")
+    s = torch.cuda.current_stream()
+    for _ in range(3):
+        pkg.dsmem_hist_partials(keys, num_bins, plan, partials, 0, s)
+        bins = pkg.dsmem_hist_reduce(partials, 1, plan["partial_stride"], num_bins, stream=s)
+        torch.cuda.synchronize()
+        assert np.array_equal(to_np(bins), want)
+    assert pkg.dsmem_hist_device_status() == 0
+
+
 def test_errors_on_device():
     d = torch.zeros(16, dtype=torch.int32, device="cuda")
     with pytest.raises(pkg.DsmemHistError) as e:
