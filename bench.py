@@ -359,7 +359,7 @@ def run_ours(a, world, rank, local):
         hint = {"hot_bin": gen.hot_bin(num_bins, seed)}
         cfg["hot_bin_hint"] = hint["hot_bin"]
     plan = pkg.dsmem_hist_plan(num_bins, n, cluster_size=P, **hint)
-    partials = torch.empty(plan["workspace_bytes"] // 4, dtype=torch.int32,
+    partials = torch.empty(plan["num_clusters"] * plan["partial_stride"], dtype=torch.int32,
                            device=dev)
     bins = torch.empty(num_bins, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)

@@ -312,12 +312,10 @@ def plan_struct(plan: dict) -> Plan:
 def dsmem_hist_partials(keys, num_bins: int, plan: dict, partials, accumulate: int = 0,
                         stream=None):
     """Stage 1: per-cluster partial rows into caller-owned `partials` (a
-    16-byte aligned CUDA 32-bit tensor of workspace_bytes / 4 elements: the
-    num_clusters * partial_stride partial rows, then the ship kernel's tile
-    counters)."""
+    16-byte aligned CUDA 32-bit tensor of num_clusters * partial_stride)."""
     import torch
     _check_keys(keys, num_bins)
-    need = plan["workspace_bytes"] // 4
+    need = plan["num_clusters"] * plan["partial_stride"]
     if not partials.is_cuda or partials.element_size() != 4 or partials.numel() < need or \
             not partials.is_contiguous():
         raise ValueError(f"partials must be a contiguous CUDA 32-bit tensor of >= {need}")

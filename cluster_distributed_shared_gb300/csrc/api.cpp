@@ -47,11 +47,6 @@ struct DeviceState {
   cudaStream_t copy_stream = nullptr;
   cudaEvent_t ev_copied[2] = {nullptr, nullptr};
   cudaEvent_t ev_consumed[2] = {nullptr, nullptr};
-  // The global-atomic helper's stream (lowest priority) and its fork and join
-  // events; helper_call serialises their use.
-  cudaStream_t helper_stream = nullptr;
-  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
-  std::mutex helper_call;
   // Largest dynamic shared memory set so far per kernel variant: direct
   // (aggregate 0/1), ship (4 / 8 keys per thread).
   int prepared_direct[2] = {0, 0};
@@ -294,55 +289,10 @@ int prepare_locked(DeviceState* st, const dsmem_hist_plan_t& p) {
   return DSMEM_HIST_OK;
 }
 
-// Keys below which no helper runs: its launch and the fork and join cost
-// more than it adds.
-constexpr int64_t kHelperMinKeys = int64_t{1} << 24;
-
-// CTAs of the global-atomic helper for a ship plan: four per SM that the
-// plan's clusters leave idle, for single-pass plans of at least
-// kHelperMinKeys keys; 0 when DSMEM_HIST_HELPER is 0.
-int helper_ctas(const DeviceState* st, const dsmem_hist_plan_t& plan, int64_t n) {
-  if (plan.kernel != DSMEM_HIST_KERNEL_SHIP || plan.passes != 1 || n < kHelperMinKeys) return 0;
-  if (env_int("DSMEM_HIST_HELPER", 1) == 0) return 0;
-  const int idle = st->dev.sm_count - plan.num_clusters * plan.cluster_size;
-  return idle >= 4 ? 4 * idle : 0;
-}
-
-// Launches a plan.  The ship kernel's tile counters (after the partial rows)
-// are zeroed first.  With `st` non-null and helper_ctas() > 0 the helper runs
-// beside it on a second stream, forked from and joined back into `stream`:
-// row 0 is zeroed first (unless accumulating), and cluster 0 adds into it.
-cudaError_t launch_plan(const dsmem_hist_plan_t& plan, ClusterHistArgs args, cudaStream_t stream,
-                        DeviceState* st = nullptr) {
-  if (plan.kernel != DSMEM_HIST_KERNEL_SHIP) return launch_cluster_hist(plan, args, stream);
-  args.queue = args.partials + static_cast<size_t>(plan.num_clusters) * args.stride;
-  cudaError_t e = cudaMemsetAsync(args.queue, 0, static_cast<size_t>(ship_queue_bytes(plan.passes)), stream);
-  if (e != cudaSuccess) return e;
-  const int helper = st ? helper_ctas(st, plan, args.n) : 0;
-  if (helper == 0) return launch_cluster_ship(plan, args, stream);
-  if (!args.accumulate &&
-      (e = cudaMemsetAsync(args.partials, 0, sizeof(uint32_t) * args.stride, stream)) != cudaSuccess)
-    return e;
-  args.shared_row0 = 1;
-  std::lock_guard<std::mutex> g(st->helper_call);
-  if (!st->helper_stream) {
-    int lo = 0, hi = 0;
-    if ((e = cudaDeviceGetStreamPriorityRange(&lo, &hi)) != cudaSuccess ||
-        (e = cudaStreamCreateWithPriority(&st->helper_stream, cudaStreamNonBlocking, lo)) != cudaSuccess ||
-        (e = cudaEventCreateWithFlags(&st->ev_fork, cudaEventDisableTiming)) != cudaSuccess ||
-        (e = cudaEventCreateWithFlags(&st->ev_join, cudaEventDisableTiming)) != cudaSuccess)
-      return e;
-  }
-  // The clusters are launched first, so they take their SMs before the
-  // helper's CTAs fill the rest; a cluster that still finds no room starts
-  // later and simply claims less.
-  if ((e = cudaEventRecord(st->ev_fork, stream)) != cudaSuccess ||
-      (e = cudaStreamWaitEvent(st->helper_stream, st->ev_fork, 0)) != cudaSuccess ||
-      (e = launch_cluster_ship(plan, args, stream)) != cudaSuccess ||
-      (e = launch_ship_helper(args, helper, st->helper_stream)) != cudaSuccess ||
-      (e = cudaEventRecord(st->ev_join, st->helper_stream)) != cudaSuccess)
-    return e;
-  return cudaStreamWaitEvent(stream, st->ev_join, 0);
+cudaError_t launch_plan(const dsmem_hist_plan_t& plan, const ClusterHistArgs& args,
+                        cudaStream_t stream) {
+  if (plan.kernel == DSMEM_HIST_KERNEL_SHIP) return launch_cluster_ship(plan, args, stream);
+  return launch_cluster_hist(plan, args, stream);
 }
 
 // Plans for the current device, confirming the shape with the occupancy
@@ -470,8 +420,6 @@ ClusterHistArgs make_args(const dsmem_hist_plan_t& plan, const int32_t* keys, in
   a.withhold_last = env_flag("DSMEM_HIST_TEST_WITHHOLD_LAST_ROUND") ? 1u : 0u;
   a.hot_bin = plan.kernel == DSMEM_HIST_KERNEL_SHIP && plan.hot_bin >= 0
                   ? static_cast<uint32_t>(plan.hot_bin) : 0xFFFFFFFFu;
-  a.queue = nullptr;       // set by launch_plan
-  a.shared_row0 = 0;
   return a;
 }
 
@@ -513,7 +461,7 @@ int run_device(const int32_t* keys, int64_t n, int32_t num_bins, uint32_t* bins,
   uint32_t* partials = static_cast<uint32_t*>(scratch);
   ClusterHistArgs args = make_args(plan, keys, n, num_bins, partials, 0);
   args.status = sr.d_status;
-  e = launch_plan(plan, args, stream, st);
+  e = launch_plan(plan, args, stream);
   if (e == cudaSuccess)
     e = launch_reduce_partials(partials, args.stride, static_cast<uint32_t>(plan.num_clusters),
                                args.num_bins, bins, stream, hot_report.min_count,
@@ -565,9 +513,9 @@ int run_partials(const int32_t* keys, int64_t n, int32_t num_bins, const dsmem_h
     return fail(DSMEM_HIST_EINVAL, "partials must be 16-byte aligned");
   if (accumulate != 0 && accumulate != 1) return fail(DSMEM_HIST_EINVAL, "accumulate must be 0 or 1");
   SlotRef sr;
-  DeviceState* st = nullptr;
   {
     std::lock_guard<std::mutex> g(g_mutex);
+    DeviceState* st = nullptr;
     if ((rc = device_state(&st))) return rc;
     if ((rc = check_plan(st, plan, num_bins))) return rc;
     if (plan->kernel == DSMEM_HIST_KERNEL_SHIP && n >= kShipMaxKeys)
@@ -579,7 +527,7 @@ int run_partials(const int32_t* keys, int64_t n, int32_t num_bins, const dsmem_h
   // The caller's plan decides the kernel (its hot_bin included): no automatic choice.
   ClusterHistArgs args = make_args(*plan, keys, n, num_bins, partials, accumulate);
   args.status = sr.d_status;
-  const cudaError_t e = launch_plan(*plan, args, stream, st);
+  const cudaError_t e = launch_plan(*plan, args, stream);
   return e == cudaSuccess ? DSMEM_HIST_OK : fail_cuda(e, "cluster histogram launch");
 }
 
@@ -672,7 +620,7 @@ int run_host(const int32_t* h_keys, int64_t n, int32_t num_bins, uint32_t* h_bin
     }
     ClusterHistArgs args = make_args(plan, stage[b], cnt, num_bins, partials, j > 0);
     args.status = sr.d_status;
-    if ((e = launch_plan(plan, args, stream, st)) != cudaSuccess ||
+    if ((e = launch_plan(plan, args, stream)) != cudaSuccess ||
         (e = cudaEventRecord(st->ev_consumed[b], stream)) != cudaSuccess) {
       rc = fail_cuda(e, "cluster histogram launch");
       break;
@@ -702,8 +650,7 @@ int run_host(const int32_t* h_keys, int64_t n, int32_t num_bins, uint32_t* h_bin
 
 // For the entry point with caller-free scratch (static_scratch.cu): the same
 // argument checks, plan and launches as dsmem_hist, with the partial rows in
-// memory the caller of this function supplies, at most `max_rows_bytes`,
-// followed by kFixedQueueBytes for the ship kernel's tile counters.
+// memory the caller of this function supplies, at most `max_rows_bytes`.
 int run_with_fixed_scratch(const int32_t* keys, int64_t n, int32_t num_bins, uint32_t* bins,
                            uint32_t* scratch, int64_t max_rows_bytes, cudaStream_t stream) {
   int rc = check_args(keys, n, num_bins, bins);
@@ -727,15 +674,7 @@ int run_with_fixed_scratch(const int32_t* keys, int64_t n, int32_t num_bins, uin
     if ((rc = stream_slot(st, stream, false, &sr))) return rc;
     if ((rc = take_pending_timeout(sr.h_status))) return rc;
     if ((rc = plan_locked(st, num_bins, n, nullptr, &plan))) return rc;
-    // The rows must fit max_rows_bytes; the ship kernel's tile counters go
-    // to the kFixedQueueBytes after them.
-    const auto rows_bytes = [](const dsmem_hist_plan_t& p) {
-      return static_cast<int64_t>(p.num_clusters) * p.partial_stride * 4;
-    };
-    if (ship_queue_bytes(plan.passes) > kFixedQueueBytes)
-      return fail(DSMEM_HIST_EINVAL, "static scratch: %d passes need more tile counters than it holds",
-                  plan.passes);
-    if (rows_bytes(plan) > max_rows_bytes) {
+    if (plan.workspace_bytes > max_rows_bytes) {
       // Fewer clusters, so their partial rows fit the static scratch.  The
       // forced count is below the automatic one (whose rows did not fit), so
       // it never exceeds the clusters that can be resident or the rows the
@@ -747,7 +686,7 @@ int run_with_fixed_scratch(const int32_t* keys, int64_t n, int32_t num_bins, uin
                     "automatic %d clusters", req.num_clusters, static_cast<long long>(row_bytes),
                     auto_clusters);
       if ((rc = plan_locked(st, num_bins, n, &req, &plan))) return rc;
-      if (plan.num_clusters > req.num_clusters || rows_bytes(plan) > max_rows_bytes)
+      if (plan.num_clusters > req.num_clusters || plan.workspace_bytes > max_rows_bytes)
         return fail(DSMEM_HIST_EINVAL, "static scratch: forced plan exceeds the scratch");
     }
     const int32_t chosen = choose_hot_bin(st, sr, n, num_bins, &hot_report);
@@ -1001,14 +940,6 @@ void dsmem_hist_release(void) {
       st->status_slot.clear();
       for (int i = 0; i < kStatusSlots; ++i)
         st->slot_seq[i] = st->slot_bins_since[i] = 0, st->slot_bins[i] = 0;
-    }
-    if (st->helper_stream) {
-      cudaStreamSynchronize(st->helper_stream);
-      cudaStreamDestroy(st->helper_stream);
-      cudaEventDestroy(st->ev_fork);
-      cudaEventDestroy(st->ev_join);
-      st->helper_stream = nullptr;
-      st->ev_fork = st->ev_join = nullptr;
     }
     if (st->copy_stream) {
       cudaStreamDestroy(st->copy_stream);

@@ -305,27 +305,18 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
   const uint32_t buf_bytes = P * c.blk;   // one staging or inbox buffer
   const uint32_t inbox0 = stage0 + 2u * buf_bytes;
 
-  // Key stream: warp tiles of 32 vectors (tile t = vectors 32t .. 32t+31).
-  // Work is claimed, not assigned: a cluster takes a chunk of `chunk` tiles
-  // per round from the pass's counter a.queue[pass] (one atomic by CTA 0), and
-  // warp w of rank q takes the chunk's kTiles consecutive tiles from
-  // (q * kWarps + w) * kTiles.  CTA 0's thread 0 writes the chunk start of
-  // round r + 3 into every CTA's ring early in round r, and its warp's
-  // arrival on the round's cluster barrier is a release, so every CTA reads
-  // it after the barrier's wait: all CTAs see the same starts whatever else
-  // happens, and the rounds run while the start is below ntiles.  Any other
-  // kernel that takes tiles from the same counter (the global-atomic helper
-  // on the SMs the clusters leave idle) shares the work the same way.  Tile
-  // indices fit 32 bits (the library keeps n below 2^38 for this kernel).
+  // Key stream: warp tiles of 32 vectors (tile t = vectors 32t .. 32t+31),
+  // kKpt/4 consecutive tiles per warp per round; tile indices fit 32 bits with room for
+  // three rounds on top (the library keeps n below 2^38 for this kernel).
   constexpr uint32_t kWarps = kShipThreads / 32;
   const uint32_t nwarps = gridDim.x * kWarps;
   const uint32_t gwarp = blockIdx.x * kWarps + warp;
   const uint32_t ntiles = static_cast<uint32_t>(((a.n - a.head) >> 2) >> 5);
   const int4* vec = reinterpret_cast<const int4*>(a.keys + a.head) + c.lane;
   constexpr int kTiles = kKpt / 4;
-  const uint32_t chunk = P * kWarps * kTiles;               // tiles per cluster and round
-  const uint32_t wofs = (rank * kWarps + warp) * kTiles;   // this warp's first tile of a chunk
-  const uint32_t ring = header0 + 224u;  // u32[4]: chunk start of round x in slot x % 4
+  const uint32_t per_round = nwarps * kTiles;
+  const uint32_t wtile0 = gwarp * kTiles;  // this warp's first tile of round 0
+  const uint32_t rounds = static_cast<uint32_t>((static_cast<uint64_t>(ntiles) + per_round - 1) / per_round);
 
   // Ship and apply: warp w serves owner (and sender) w mod P, as member sg of
   // the sng warps that do; lane l of member sg starts at vector 32*sg + l of
@@ -380,40 +371,20 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
       mbar_init(staged, kWarps);
       fence_mbar_init();
     }
-    if (rank == 0 && threadIdx.x == 0) {
-      // The pass's rounds 0 .. 3, into every CTA's ring (published by the
-      // barrier below).
-      const uint32_t s0 = atomicAdd(a.queue + pass, 5u * chunk);
-      const uint4 v = make_uint4(s0, s0 + chunk, s0 + 2u * chunk, s0 + 3u * chunk);
-      for (uint32_t q = 0; q < P; ++q) st_cluster_v4(map_rank(ring, q), v);
-    }
-    cluster_barrier();  // slices zeroed, mbarriers initialised, rounds 0 .. 3 claimed cluster-wide
+    cluster_barrier();  // slices zeroed and mbarriers initialised cluster-wide
 
-    // Chunk starts of rounds r and r + 1 (every thread keeps its own copy);
-    // CTA 0's thread 0 also keeps the last start it claimed.
-    uint32_t c0 = ld_shared_u32(ring), c1 = ld_shared_u32(ring + 4u);
-    uint32_t pending = ld_shared_u32(ring + 12u) + chunk;  // CTA 0's thread 0: the start of round 4
     int4 cur[kTiles];
-    if (c0 < ntiles) {
-      load_round<kKpt>(cur, vec, ntiles, c0 + wofs, c0 + chunk > ntiles);
+    if (rounds > 0) {
+      load_round<kKpt>(cur, vec, ntiles, wtile0, rounds == 1);
       c.cur_lane = cur_lane0;
       c.lim0 = stage0 + c.blk;
       partition_round<kTiles, kPow2, kSkew>(cur, c, hot_keys);
-      if (c1 < ntiles) load_round<kKpt>(cur, vec, ntiles, c1 + wofs, c1 + chunk > ntiles);
+      if (rounds > 1) load_round<kKpt>(cur, vec, ntiles, wtile0 + per_round, rounds == 2);
     }
     __syncthreads();  // round 0 staged
     uint32_t k = 0;  // r % 3
-    uint32_t r = 0;
-    for (; c0 < ntiles; ++r) {
+    for (uint32_t r = 0; r < rounds; ++r) {
       const uint32_t b = r & 1u;
-      if (rank == 0 && threadIdx.x == 0 && r > 0) {
-        // The start of round r + 3 (rounds 0 .. 3 went out with the pass),
-        // to every CTA's ring slot (r + 3) % 4, which held round r - 1: every
-        // CTA has passed this barrier's wait of round r - 1, so none still
-        // reads it.  Then claim round r + 4, unless the counter has run out.
-        for (uint32_t q = 0; q < P; ++q) st_cluster_u32(map_rank(ring + 4u * ((r + 3u) & 3u), q), pending);
-        if (pending < ntiles) pending = atomicAdd(a.queue + pass, chunk);
-      }
       if (r > 0 && so != rank) {
         // Apply sender so's block of round r - 1, once every sender has
         // arrived and every byte has landed (this CTA's own block was
@@ -433,12 +404,7 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
       // Relaxed: inbox data is published through the mbarriers; this
       // barrier only tells senders that round r-1's inbox has been read
       // (every load of it has returned: its values fed the reds above).
-      // CTA 0's warp 0 releases: its chunk start of round r + 3 is read after
-      // this barrier's wait.
-      if (rank == 0 && warp == 0)
-        cluster_arrive_release();
-      else
-        cluster_arrive_relaxed();
+      cluster_arrive_relaxed();
       // Set (r + 2) % 3 was last read by round r - 1's ship, which every warp
       // finished before the wait above; round r + 2 partitions with it into
       // buffer b, after the wait of round r + 1.
@@ -456,7 +422,7 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
             apply_vector(c.slice, ld_shared_v4(at));
             st_shared_v4(at, pad);
           }
-        } else if (!(a.withhold_last && c1 >= ntiles)) {
+        } else if (!(a.withhold_last && r + 1u == rounds)) {
           const uint32_t mbar = full_out + 8u * b;
           if (sg == 0 && c.lane == 0) {
             mbar_arrive_expect_tx_remote(mbar, 64u * rows + 4u);
@@ -468,29 +434,24 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
           }
         }
       }
-      // Start of round r + 2: written in round r - 1 before a release
-      // arrival whose wait every thread has passed (rounds 0 .. 3: with the
-      // pass's first barrier).
-      const uint32_t c2 = ld_shared_u32(ring + 4u * ((r + 2u) & 3u));
       const uint32_t k1 = k == 2 ? 0u : k + 1u;
-      if (c1 < ntiles) {
+      if (r + 1 < rounds) {
         // Partition round r + 1 into the other buffer while other warps
         // still ship and apply round r; then load round r + 2.
         c.cur_lane = cur_lane0 + k1 * set_bytes;
         c.lim0 = stage0 + (b ^ 1u) * buf_bytes + c.blk;
         partition_round<kTiles, kPow2, kSkew>(cur, c, hot_keys);
-        if (c2 < ntiles) load_round<kKpt>(cur, vec, ntiles, c2 + wofs, c2 + chunk > ntiles);
+        if (r + 2 < rounds)
+          load_round<kKpt>(cur, vec, ntiles, wtile0 + (r + 2) * per_round, r + 3 == rounds);
         __syncwarp();  // the warp's staging stores and cursor updates precede the arrival
         if (c.lane == 0) mbar_arrive_local(staged);
       }
       cluster_wait();   // round r's inboxes complete everywhere
       k = k1;
-      c0 = c1;
-      c1 = c2;
     }
-    if (r > 0 && so != rank) {
-      const uint32_t pb = (r - 1u) & 1u;
-      if (wait_mbar(full0 + 8u * pb, ((r - 1u) >> 1) & 1u, gave_up, a.wait_cycles, a.status)) {
+    if (rounds > 0 && so != rank) {
+      const uint32_t pb = (rounds - 1u) & 1u;
+      if (wait_mbar(full0 + 8u * pb, ((rounds - 1u) >> 1) & 1u, gave_up, a.wait_cycles, a.status)) {
         const uint32_t src = src0 + pb * buf_bytes;
         const uint32_t end = src - vofs + 64u * min(ld_shared_u32(hdr_in + 64u * pb), qs);
         for (uint32_t at = src; at < end; at += step) apply_vector(c.slice, ld_shared_v4(at));
@@ -547,17 +508,6 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
       const uint32_t cnt = c.range - rank * c.S < c.S ? c.range - rank * c.S : c.S;
       uint4* dst = reinterpret_cast<uint4*>(a.partials + static_cast<size_t>(cid) * a.stride + first);
       const uint32_t nv = (cnt + 3) / 4;
-      if (a.shared_row0 && cid == 0) {
-        // Row 0 also receives the helper kernel's atomics.
-        uint32_t* d = reinterpret_cast<uint32_t*>(dst);
-        for (uint32_t i = threadIdx.x; i < nv; i += blockDim.x) {
-          const uint4 v = s4[i];
-          if (v.x) red_add_global(d + 4u * i, v.x);
-          if (v.y) red_add_global(d + 4u * i + 1u, v.y);
-          if (v.z) red_add_global(d + 4u * i + 2u, v.z);
-          if (v.w) red_add_global(d + 4u * i + 3u, v.w);
-        }
-      } else
       for (uint32_t i = threadIdx.x; i < nv; i += blockDim.x) {
         uint4 v = s4[i];
         if (a.accumulate) {
@@ -571,35 +521,6 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
       }
     }
     if (pass + 1 < a.passes) __syncthreads();
-  }
-}
-
-// The helper beside a single-pass launch, on the SMs its clusters leave idle
-// (clusters of 8 fit only 15 times in this GPU's 152 SMs): it claims
-// kHelperTiles tiles at a time from the clusters' counter and adds their
-// in-range keys to partial row 0 with global atomics, the comparison
-// kernel's method ("Distributed Shared Memory", section "When it beats
-// global atomics").  Since both sides claim from one counter, each takes
-// what its speed allows: on keys with hot bins, whose global atomics
-// serialise, the helper takes little.
-__global__ void __launch_bounds__(kHelperThreads) ship_helper_kernel(const ClusterHistArgs a) {
-  __shared__ uint32_t s_t0;
-  const uint32_t ntiles = static_cast<uint32_t>(((a.n - a.head) >> 2) >> 5);
-  const int4* vec = reinterpret_cast<const int4*>(a.keys + a.head);
-  for (;;) {
-    if (threadIdx.x == 0) s_t0 = atomicAdd(a.queue, kHelperTiles);
-    __syncthreads();
-    const uint32_t t0 = s_t0;
-    __syncthreads();
-    if (t0 >= ntiles) break;
-    const uint32_t t1 = min(t0 + kHelperTiles, ntiles);
-    for (uint64_t v = 32ull * t0 + threadIdx.x; v < 32ull * t1; v += blockDim.x) {
-      const int4 k = ld_stream_v4(vec + v);
-      if (static_cast<uint32_t>(k.x) < a.num_bins) red_add_global(a.partials + k.x, 1u);
-      if (static_cast<uint32_t>(k.y) < a.num_bins) red_add_global(a.partials + k.y, 1u);
-      if (static_cast<uint32_t>(k.z) < a.num_bins) red_add_global(a.partials + k.z, 1u);
-      if (static_cast<uint32_t>(k.w) < a.num_bins) red_add_global(a.partials + k.w, 1u);
-    }
   }
 }
 
@@ -662,11 +583,6 @@ cudaError_t query_ship_potential_cluster_size(int kpt, int smem_bytes, int* out)
   cfg.blockDim = dim3(kShipThreads, 1, 1);
   cfg.dynamicSmemBytes = smem_bytes;
   return cudaOccupancyMaxPotentialClusterSize(out, ship_kernel_ptr(kpt, true, false), &cfg);
-}
-
-cudaError_t launch_ship_helper(const ClusterHistArgs& args, int ctas, cudaStream_t stream) {
-  ship_helper_kernel<<<static_cast<unsigned>(ctas), kHelperThreads, 0, stream>>>(args);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_cluster_ship(const dsmem_hist_plan_t& plan, const ClusterHistArgs& args,

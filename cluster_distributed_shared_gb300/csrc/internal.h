@@ -54,26 +54,7 @@ struct ClusterHistArgs {
   long long wait_cycles;    // bound of one inbox wait (clock64 cycles)
   uint32_t withhold_last;   // test only: senders skip the last round's arrival and stores
   uint32_t hot_bin;         // ship kernel: the plan's hot bin, 0xFFFFFFFF for none
-  // Ship kernel: per-pass tile counters (u32[passes], zero at launch) from
-  // which clusters claim their rounds' tiles, and whether a helper kernel
-  // adds into partial row 0 at the same time (then cluster 0 adds its slice
-  // with atomics instead of storing it).
-  uint32_t* queue;
-  uint32_t shared_row0;
 };
-
-// Bytes of the ship kernel's per-pass tile counters, after the partial rows
-// in the workspace.
-inline int64_t ship_queue_bytes(int passes) { return 16 * ((static_cast<int64_t>(passes) + 3) / 4); }
-
-// Bytes after the rows of a fixed scratch (the allocation-free entry point)
-// that hold the tile counters: up to 1024 passes.
-constexpr int64_t kFixedQueueBytes = 4096;
-
-// The global-atomic helper that runs beside a ship launch on the SMs its
-// clusters leave idle: tiles per claim and threads per CTA.
-constexpr uint32_t kHelperTiles = 32;
-constexpr int kHelperThreads = 512;
 
 // Streams per device with their own status words (later streams share the
 // last slot).
@@ -93,9 +74,6 @@ cudaError_t launch_reduce_partials(const uint32_t* partials, uint64_t stride,
                                    cudaStream_t stream, uint32_t hot_min = 0,
                                    unsigned long long* hot_word = nullptr,
                                    uint32_t* seq_word = nullptr, uint32_t seq = 0);
-// The helper: `ctas` CTAs claim tiles of args.queue[0] and add their keys to
-// partial row 0 with global atomics (single-pass plans only).
-cudaError_t launch_ship_helper(const ClusterHistArgs& args, int ctas, cudaStream_t stream);
 cudaError_t launch_global_atomic(const int32_t* keys, int64_t n, uint32_t num_bins,
                                  uint32_t* bins, cudaStream_t stream);
 // Work-free control kernel with a plan's grid, cluster and shared memory.

@@ -216,8 +216,7 @@ int plan_shape(const dsmem_hist_device_t* dev, int32_t num_bins, int64_t n,
     out->hot_bin = req->hot_bin;
   }
   out->partial_stride = stride;
-  out->workspace_bytes = C * stride * 4 +
-                        (kernel == DSMEM_HIST_KERNEL_SHIP ? ship_queue_bytes(out->passes) : 0);
+  out->workspace_bytes = C * stride * 4;
   return DSMEM_HIST_OK;
 }
 

@@ -42,12 +42,6 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
   __syncwarp();
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
-// The arrival with release ordering: this thread's earlier writes (local or
-// to other CTAs' shared memory) are visible to every thread after its wait.
-__device__ __forceinline__ void cluster_arrive_release() {
-  __syncwarp();
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
 __device__ __forceinline__ void cluster_wait() {
   __syncwarp();
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -116,9 +110,6 @@ __device__ __forceinline__ uint32_t map_rank(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void red_add_cluster(uint32_t cluster_addr, uint32_t v) {
   asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v));
 }
-__device__ __forceinline__ void red_add_global(uint32_t* p, uint32_t v) {
-  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 __device__ __forceinline__ void red_add_local(uint32_t cta_addr, uint32_t v) {
   asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(cta_addr), "r"(v));
 }
@@ -132,9 +123,6 @@ __device__ __forceinline__ uint32_t atom_add_local(uint32_t cta_addr, uint32_t v
 // their order relative to each other and to the barriers above (which do
 // clobber memory); plain C++ shared-memory accesses are separated from them by
 // those barriers.
-__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
-}
 __device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, const uint4& v) {
   asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(v.x),
                "r"(v.y), "r"(v.z), "r"(v.w));

@@ -25,10 +25,9 @@ namespace {
 
 // 32 MiB of partial rows: one row of num_bins counters (rounded up to a
 // multiple of 4) per cluster, so up to 8,388,608 bins, and as many clusters
-// as fit for smaller bin counts (15 rows of 262,144 bins need 15 MiB); then
-// the ship kernel's per-pass tile counters.
+// as fit for smaller bin counts (15 rows of 262,144 bins need 15 MiB).
 constexpr int64_t kStaticScratchBytes = int64_t{32} << 20;
-static __device__ __align__(256) uint32_t g_static_partials[(kStaticScratchBytes + kFixedQueueBytes) / 4];
+static __device__ __align__(256) uint32_t g_static_partials[kStaticScratchBytes / 4];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_static_mutex;

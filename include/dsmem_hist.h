@@ -113,9 +113,7 @@ typedef struct dsmem_hist_plan {
                                   dsmem_hist_request_t.hot_bin).  -1: none.  The planner sets it
                                   only on request; dsmem_hist_partials uses it as given */
   int64_t partial_stride;      /* u32 elements between two clusters' partial rows (num_bins rounded up to 4) */
-  int64_t workspace_bytes;     /* scratch: num_clusters * partial_stride * 4 bytes of partial
-                                  rows, then (ship kernel) 16 bytes per 4 passes of tile
-                                  counters */
+  int64_t workspace_bytes;     /* scratch: num_clusters * partial_stride * 4 */
 } dsmem_hist_plan_t;
 
 /* Planner overrides; a zero field (or -1 for `aggregate` and `kernel`) means "choose". */
@@ -203,17 +201,9 @@ DSMEM_HIST_API int dsmem_hist_host(const int32_t* h_keys, int64_t n, int32_t num
  * barrier, flush).
  *   plan      from dsmem_hist_plan for the same num_bins (checked for
  *             consistency; EINVAL otherwise)
- *   partials  device, 16-byte aligned, plan->workspace_bytes bytes: the
- *             num_clusters * partial_stride uint32 partial rows, then the ship
- *             kernel's tile counters, which the call zeroes (clusters claim
- *             their rounds' keys from them).  With accumulate == 1 the rows
- *             must hold those of an earlier call with the same plan (used to
- *             fold key chunks into one histogram)
- * For a single-pass ship plan of at least 2^24 keys whose clusters leave SMs
- * idle, a global-atomic helper kernel runs beside the clusters on those SMs,
- * on a second stream of the library forked from and joined back into
- * `stream`; it takes keys from the same tile counters and adds them to row 0
- * (DSMEM_HIST_HELPER=0 in the environment turns it off).
+ *   partials  device, 16-byte aligned, num_clusters * partial_stride uint32;
+ *             with accumulate == 1 it must hold the rows of an earlier call
+ *             with the same plan (used to fold key chunks into one histogram)
  * Asynchronous on `stream`. */
 DSMEM_HIST_API int dsmem_hist_partials(const int32_t* keys, int64_t n, int32_t num_bins,
                                        const dsmem_hist_plan_t* plan, uint32_t* partials,

@@ -96,7 +96,7 @@ def test_partials_entry_reports_a_timeout_of_an_earlier_launch(monkeypatch):
     keys_np = gen.uniform(n, num_bins, seed=72)
     keys = torch.from_numpy(keys_np).cuda()
     plan = pkg.dsmem_hist_plan(num_bins, n, cluster_size=2, kernel=pkg.KERNEL_SHIP)
-    partials = torch.empty(plan["workspace_bytes"] // 4, dtype=torch.int32,
+    partials = torch.empty(plan["num_clusters"] * plan["partial_stride"], dtype=torch.int32,
                            device="cuda")
     s = torch.cuda.Stream()
     monkeypatch.setenv("DSMEM_HIST_TEST_WITHHOLD_LAST_ROUND", "1")

@@ -342,7 +342,7 @@ def test_long_round_chains_in_one_cluster(P, kpt):
     plan["keys_per_thread"] = kpt
     rounds = n // (P * pkg.SHIP_THREADS * kpt)
     assert plan["num_clusters"] == 1 and plan["bins_per_cta"] == 32768 and rounds >= 70
-    partials = torch.empty(plan["workspace_bytes"] // 4, dtype=torch.int32, device="cuda")
+    partials = torch.empty(plan["partial_stride"], dtype=torch.int32, device="cuda")
     s = torch.cuda.current_stream()
     for _ in range(3):
         pkg.dsmem_hist_partials(keys, num_bins, plan, partials, 0, s)
@@ -442,7 +442,7 @@ def test_hot_bin_hint_is_exact(share):
     plan = pkg.dsmem_hist_plan(num_bins, n, cluster_size=2, hot_bin=hb)
     assert plan["hot_bin"] == hb and plan["passes"] == 4   # the hot bin lies in one of four passes
     # through the two-stage entry points with the hinted plan
-    partials = torch.empty(plan["workspace_bytes"] // 4, dtype=torch.int32,
+    partials = torch.empty(plan["num_clusters"] * plan["partial_stride"], dtype=torch.int32,
                            device="cuda")
     pkg.dsmem_hist_partials(d, num_bins, plan, partials)
     got = to_np(pkg.dsmem_hist_reduce(partials, plan["num_clusters"], plan["partial_stride"],
