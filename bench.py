@@ -359,14 +359,14 @@ def run_ours(a, world, rank, local):
         hint = {"hot_bin": gen.hot_bin(num_bins, seed)}
         cfg["hot_bin_hint"] = hint["hot_bin"]
     plan = pkg.dsmem_hist_plan(num_bins, n, cluster_size=P, **hint)
-    partials = torch.empty(plan["num_clusters"] * plan["partial_stride"], dtype=torch.int32,
+    partials = torch.empty(-(-plan["workspace_bytes"] // 4), dtype=torch.int32,
                            device=dev)
     bins = torch.empty(num_bins, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
         pkg.dsmem_hist_partials(keys, num_bins, plan, partials, 0, stream)
-        pkg.dsmem_hist_reduce(partials, plan["num_clusters"], plan["partial_stride"], num_bins,
+        pkg.dsmem_hist_reduce(partials, plan["partial_rows"], plan["partial_stride"], num_bins,
                               bins, stream)
 
     for _ in range(a.warmup):
@@ -403,7 +403,7 @@ def run_ours(a, world, rank, local):
         ev_k[k][0].record(stream)
         pkg.dsmem_hist_partials(keys, num_bins, plan, partials, 0, stream)
         ev_k[k][1].record(stream)
-        pkg.dsmem_hist_reduce(partials, plan["num_clusters"], plan["partial_stride"], num_bins,
+        pkg.dsmem_hist_reduce(partials, plan["partial_rows"], plan["partial_stride"], num_bins,
                               bins, stream)
     ev_end.record(stream)
     torch.cuda.synchronize(dev)

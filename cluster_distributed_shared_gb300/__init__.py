@@ -52,6 +52,7 @@ class Plan(ctypes.Structure):
         ("keys_per_thread", ctypes.c_int32),
         ("sub_vectors", ctypes.c_int32),
         ("hot_bin", ctypes.c_int32),
+        ("partial_rows", ctypes.c_int32),
         ("partial_stride", ctypes.c_int64),
         ("workspace_bytes", ctypes.c_int64),
     ]
@@ -311,11 +312,14 @@ def plan_struct(plan: dict) -> Plan:
 
 def dsmem_hist_partials(keys, num_bins: int, plan: dict, partials, accumulate: int = 0,
                         stream=None):
-    """Stage 1: per-cluster partial rows into caller-owned `partials` (a
-    16-byte aligned CUDA 32-bit tensor of num_clusters * partial_stride)."""
+    """Stage 1: partial rows into caller-owned `partials` (a 16-byte aligned
+    CUDA 32-bit tensor of workspace_bytes / 4 elements: partial_rows rows of
+    partial_stride, then the helper's tile counter when the plan has a
+    helper row); sum them with dsmem_hist_reduce(partials,
+    plan["partial_rows"], ...)."""
     import torch
     _check_keys(keys, num_bins)
-    need = plan["num_clusters"] * plan["partial_stride"]
+    need = -(-plan["workspace_bytes"] // 4)
     if not partials.is_cuda or partials.element_size() != 4 or partials.numel() < need or \
             not partials.is_contiguous():
         raise ValueError(f"partials must be a contiguous CUDA 32-bit tensor of >= {need}")
@@ -327,16 +331,17 @@ def dsmem_hist_partials(keys, num_bins: int, plan: dict, partials, accumulate: i
     return partials
 
 
-def dsmem_hist_reduce(partials, num_clusters: int, partial_stride: int, num_bins: int, out=None,
+def dsmem_hist_reduce(partials, num_rows: int, partial_stride: int, num_bins: int, out=None,
                       stream=None):
-    """Stage 2: sum the partial rows into `num_bins` counts."""
+    """Stage 2: sum the first `num_rows` partial rows (a plan's partial_rows)
+    into `num_bins` counts."""
     import torch
     if not partials.is_cuda or partials.element_size() != 4 or \
-            partials.numel() < num_clusters * partial_stride:
+            partials.numel() < num_rows * partial_stride:
         raise ValueError("partials too small")
     out = _out_bins(partials, num_bins, out)
     with torch.cuda.device(partials.device):
-        _check(lib().dsmem_hist_reduce(partials.data_ptr(), int(num_clusters), int(partial_stride),
+        _check(lib().dsmem_hist_reduce(partials.data_ptr(), int(num_rows), int(partial_stride),
                                        int(num_bins), out.data_ptr(), _stream_handle(stream)))
     return out
 

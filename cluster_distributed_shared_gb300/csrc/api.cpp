@@ -56,6 +56,12 @@ struct DeviceState {
   // (kernel, variant, threads, smem) -> largest co-schedulable cluster size
   std::map<std::tuple<int, int, int, int>, int> potential;
   std::mutex host_call;  // serialises dsmem_hist_host on this device
+  // The helper kernel's stream (lowest priority, so the clusters launched
+  // first keep their SMs) and its fork and join events; helper_call
+  // serialises their use.
+  cudaStream_t helper_stream = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  std::mutex helper_call;
   // Per-stream words in pinned, host-mapped memory (h_status on the host,
   // d_status the same memory for the device), kStatusSlots of each kind: the
   // ship kernel's u32 status words; u32 sequence stamps, the number of the
@@ -235,6 +241,7 @@ int32_t choose_hot_bin(DeviceState* st, const SlotRef& r, int64_t n, int32_t num
 void use_hot_bin(dsmem_hist_plan_t* plan, int32_t chosen, const SlotRef& r) {
   if (chosen < 0 || plan->kernel != DSMEM_HIST_KERNEL_SHIP) return;
   plan->hot_bin = chosen;
+  set_partial_rows(plan, false);  // a hot bin would serialise the helper's atomics
   if (trace_enabled())
     fprintf(stderr, "[dsmem_hist] stream slot %d: bin %d held a sixth or more of the keys of a "
             "recent histogram -> hot-bin kernel\n", r.slot, chosen);
@@ -289,10 +296,63 @@ int prepare_locked(DeviceState* st, const dsmem_hist_plan_t& p) {
   return DSMEM_HIST_OK;
 }
 
-cudaError_t launch_plan(const dsmem_hist_plan_t& plan, const ClusterHistArgs& args,
-                        cudaStream_t stream) {
-  if (plan.kernel == DSMEM_HIST_KERNEL_SHIP) return launch_cluster_ship(plan, args, stream);
-  return launch_cluster_hist(plan, args, stream);
+// The helper's speed per idle SM relative to a cluster SM's (global atomics
+// against the ship kernel, measured on uniform keys: about 1.5 against 4.3
+// G keys/s per SM); it sets the helper's share of the tiles.
+constexpr double kHelperRelativeRate = 0.35;
+
+// Launches a plan.  With `st` non-null and a helper row in the plan
+// (partial_rows > num_clusters), the ship kernel's rounds cover the first
+// tiles and the global-atomic helper, on the SMs the clusters leave idle,
+// takes the rest: its share is what the idle SMs would finish in the time
+// the clusters take for theirs, and the clusters' rounds are rounded down
+// to whole rounds.  The helper runs on a second stream forked from and
+// joined back into `stream`; the tile counter is zeroed on `stream` before
+// the fork and the helper's row on the helper stream (unless accumulating).
+cudaError_t launch_plan(const dsmem_hist_plan_t& plan, ClusterHistArgs args, cudaStream_t stream,
+                        DeviceState* st = nullptr) {
+  if (plan.kernel != DSMEM_HIST_KERNEL_SHIP) return launch_cluster_hist(plan, args, stream);
+  const uint32_t ntiles = static_cast<uint32_t>(((args.n - args.head) >> 2) >> 5);
+  args.cluster_tiles = ntiles;
+  args.helper_tiles = 0;
+  args.queue = nullptr;
+  if (!st || plan.partial_rows <= plan.num_clusters) return launch_cluster_ship(plan, args, stream);
+
+  cudaError_t e;
+  std::lock_guard<std::mutex> g(st->helper_call);
+  if (!st->helper_stream) {
+    int least = 0, greatest = 0;
+    if ((e = prepare_ship_helper()) != cudaSuccess ||
+        (e = cudaDeviceGetStreamPriorityRange(&least, &greatest)) != cudaSuccess ||
+        (e = cudaStreamCreateWithPriority(&st->helper_stream, cudaStreamNonBlocking, least)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&st->ev_fork, cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&st->ev_join, cudaEventDisableTiming)) != cudaSuccess)
+      return e;
+  }
+  const int active = plan.num_clusters * plan.cluster_size;
+  const int idle = st->dev.sm_count > active ? st->dev.sm_count - active : 0;
+  double share = idle * kHelperRelativeRate / (active + idle * kHelperRelativeRate);
+  if (const char* v = getenv("DSMEM_HIST_HELPER_SHARE")) share = atof(v);  // sweeps
+  share = share < 0.0 ? 0.0 : (share > 1.0 ? 1.0 : share);
+  const uint64_t per_round = static_cast<uint64_t>(active) * (kShipThreads / 32) * (plan.keys_per_thread / 4);
+  args.cluster_tiles = static_cast<uint32_t>(
+      static_cast<uint64_t>(static_cast<double>(ntiles) * (1.0 - share)) / per_round * per_round);
+  args.helper_tiles = ntiles - args.cluster_tiles;
+  uint32_t* row = args.partials + static_cast<size_t>(plan.num_clusters) * args.stride;
+  args.queue = args.partials + static_cast<size_t>(plan.partial_rows) * args.stride;
+  // The clusters are launched first, so they take their SMs before the
+  // helper's CTAs fill the idle ones; a cluster that still finds no room
+  // starts later, and the mop-up balances the work either way.
+  if ((e = cudaMemsetAsync(args.queue, 0, 16, stream)) != cudaSuccess ||
+      (e = cudaEventRecord(st->ev_fork, stream)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(st->helper_stream, st->ev_fork, 0)) != cudaSuccess ||
+      (!args.accumulate &&
+       (e = cudaMemsetAsync(row, 0, sizeof(uint32_t) * args.stride, st->helper_stream)) != cudaSuccess) ||
+      (e = launch_cluster_ship(plan, args, stream)) != cudaSuccess ||
+      (e = launch_ship_helper(args, row, idle, st->helper_stream)) != cudaSuccess ||
+      (e = cudaEventRecord(st->ev_join, st->helper_stream)) != cudaSuccess)
+    return e;
+  return cudaStreamWaitEvent(stream, st->ev_join, 0);
 }
 
 // Plans for the current device, confirming the shape with the occupancy
@@ -373,6 +433,8 @@ int plan_locked(DeviceState* st, int32_t num_bins, int64_t n, const dsmem_hist_r
                   out->cluster_size, out->block_threads, out->smem_bytes);
     dev.max_cluster_size = out->cluster_size / 2;
   }
+  if (out->partial_rows > out->num_clusters && env_int("DSMEM_HIST_HELPER", 1) == 0)
+    set_partial_rows(out, false);
   if (trace_enabled())
     fprintf(stderr,
             "[dsmem_hist] bins=%d n=%lld -> kernel=%s P=%d S=%d passes=%d threads=%d C=%d "
@@ -420,6 +482,9 @@ ClusterHistArgs make_args(const dsmem_hist_plan_t& plan, const int32_t* keys, in
   a.withhold_last = env_flag("DSMEM_HIST_TEST_WITHHOLD_LAST_ROUND") ? 1u : 0u;
   a.hot_bin = plan.kernel == DSMEM_HIST_KERNEL_SHIP && plan.hot_bin >= 0
                   ? static_cast<uint32_t>(plan.hot_bin) : 0xFFFFFFFFu;
+  a.cluster_tiles = 0xFFFFFFFFu;  // launch_plan sets the helper's split
+  a.helper_tiles = 0;
+  a.queue = nullptr;
   return a;
 }
 
@@ -461,9 +526,9 @@ int run_device(const int32_t* keys, int64_t n, int32_t num_bins, uint32_t* bins,
   uint32_t* partials = static_cast<uint32_t*>(scratch);
   ClusterHistArgs args = make_args(plan, keys, n, num_bins, partials, 0);
   args.status = sr.d_status;
-  e = launch_plan(plan, args, stream);
+  e = launch_plan(plan, args, stream, st);
   if (e == cudaSuccess)
-    e = launch_reduce_partials(partials, args.stride, static_cast<uint32_t>(plan.num_clusters),
+    e = launch_reduce_partials(partials, args.stride, static_cast<uint32_t>(plan.partial_rows),
                                args.num_bins, bins, stream, hot_report.min_count,
                                hot_report.word, hot_report.seq_word, hot_report.seq);
   const cudaError_t ef = cudaFreeAsync(scratch, stream);
@@ -502,6 +567,11 @@ int check_plan(const DeviceState* st, const dsmem_hist_plan_t* p, int32_t num_bi
   if (p->hot_bin < -1 || p->hot_bin >= num_bins ||
       (p->hot_bin >= 0 && p->kernel != DSMEM_HIST_KERNEL_SHIP))
     return fail(DSMEM_HIST_EINVAL, "plan: hot_bin must be -1 or a bin of a ship-kernel plan");
+  if (p->partial_rows != p->num_clusters &&
+      !(p->partial_rows == p->num_clusters + 1 && p->kernel == DSMEM_HIST_KERNEL_SHIP &&
+        p->passes == 1 && p->hot_bin < 0))
+    return fail(DSMEM_HIST_EINVAL, "plan: partial_rows must be num_clusters, or num_clusters + 1 "
+                "(the helper's row) for a single-pass ship plan without a hot bin");
   return DSMEM_HIST_OK;
 }
 
@@ -513,9 +583,9 @@ int run_partials(const int32_t* keys, int64_t n, int32_t num_bins, const dsmem_h
     return fail(DSMEM_HIST_EINVAL, "partials must be 16-byte aligned");
   if (accumulate != 0 && accumulate != 1) return fail(DSMEM_HIST_EINVAL, "accumulate must be 0 or 1");
   SlotRef sr;
+  DeviceState* st = nullptr;
   {
     std::lock_guard<std::mutex> g(g_mutex);
-    DeviceState* st = nullptr;
     if ((rc = device_state(&st))) return rc;
     if ((rc = check_plan(st, plan, num_bins))) return rc;
     if (plan->kernel == DSMEM_HIST_KERNEL_SHIP && n >= kShipMaxKeys)
@@ -527,21 +597,21 @@ int run_partials(const int32_t* keys, int64_t n, int32_t num_bins, const dsmem_h
   // The caller's plan decides the kernel (its hot_bin included): no automatic choice.
   ClusterHistArgs args = make_args(*plan, keys, n, num_bins, partials, accumulate);
   args.status = sr.d_status;
-  const cudaError_t e = launch_plan(*plan, args, stream);
+  const cudaError_t e = launch_plan(*plan, args, stream, st);
   return e == cudaSuccess ? DSMEM_HIST_OK : fail_cuda(e, "cluster histogram launch");
 }
 
-int run_reduce(const uint32_t* partials, int32_t num_clusters, int64_t stride, int32_t num_bins,
+int run_reduce(const uint32_t* partials, int32_t num_rows, int64_t stride, int32_t num_bins,
                uint32_t* bins, cudaStream_t stream) {
   if (num_bins < 1) return fail(DSMEM_HIST_EINVAL, "num_bins must be >= 1");
   if (!partials || !bins) return fail(DSMEM_HIST_EINVAL, "partials and bins must not be NULL");
-  if (num_clusters < 1) return fail(DSMEM_HIST_EINVAL, "num_clusters must be >= 1");
+  if (num_rows < 1) return fail(DSMEM_HIST_EINVAL, "num_rows must be >= 1");
   if (stride < num_bins || (stride & 3))
     return fail(DSMEM_HIST_EINVAL, "partial_stride must be >= num_bins and a multiple of 4");
   if ((reinterpret_cast<uintptr_t>(partials) & 15u) || (reinterpret_cast<uintptr_t>(bins) & 3u))
     return fail(DSMEM_HIST_EINVAL, "partials must be 16-byte and bins 4-byte aligned");
   const cudaError_t e = launch_reduce_partials(partials, static_cast<uint64_t>(stride),
-                                               static_cast<uint32_t>(num_clusters),
+                                               static_cast<uint32_t>(num_rows),
                                                static_cast<uint32_t>(num_bins), bins, stream);
   return e == cudaSuccess ? DSMEM_HIST_OK : fail_cuda(e, "reduce launch");
 }
@@ -620,7 +690,7 @@ int run_host(const int32_t* h_keys, int64_t n, int32_t num_bins, uint32_t* h_bin
     }
     ClusterHistArgs args = make_args(plan, stage[b], cnt, num_bins, partials, j > 0);
     args.status = sr.d_status;
-    if ((e = launch_plan(plan, args, stream)) != cudaSuccess ||
+    if ((e = launch_plan(plan, args, stream, st)) != cudaSuccess ||
         (e = cudaEventRecord(st->ev_consumed[b], stream)) != cudaSuccess) {
       rc = fail_cuda(e, "cluster histogram launch");
       break;
@@ -628,7 +698,7 @@ int run_host(const int32_t* h_keys, int64_t n, int32_t num_bins, uint32_t* h_bin
   }
   if (rc == DSMEM_HIST_OK && n > 0) {
     if ((e = launch_reduce_partials(partials, static_cast<uint64_t>(plan.partial_stride),
-                                    static_cast<uint32_t>(plan.num_clusters),
+                                    static_cast<uint32_t>(plan.partial_rows),
                                     static_cast<uint32_t>(num_bins), d_bins, stream,
                                     hot_report.min_count, hot_report.word,
                                     hot_report.seq_word, hot_report.seq)) != cudaSuccess)
@@ -674,6 +744,8 @@ int run_with_fixed_scratch(const int32_t* keys, int64_t n, int32_t num_bins, uin
     if ((rc = stream_slot(st, stream, false, &sr))) return rc;
     if ((rc = take_pending_timeout(sr.h_status))) return rc;
     if ((rc = plan_locked(st, num_bins, n, nullptr, &plan))) return rc;
+    // No helper kernel here: it would need a stream of its own.
+    set_partial_rows(&plan, false);
     if (plan.workspace_bytes > max_rows_bytes) {
       // Fewer clusters, so their partial rows fit the static scratch.  The
       // forced count is below the automatic one (whose rows did not fit), so
@@ -686,6 +758,7 @@ int run_with_fixed_scratch(const int32_t* keys, int64_t n, int32_t num_bins, uin
                     "automatic %d clusters", req.num_clusters, static_cast<long long>(row_bytes),
                     auto_clusters);
       if ((rc = plan_locked(st, num_bins, n, &req, &plan))) return rc;
+      set_partial_rows(&plan, false);
       if (plan.num_clusters > req.num_clusters || plan.workspace_bytes > max_rows_bytes)
         return fail(DSMEM_HIST_EINVAL, "static scratch: forced plan exceeds the scratch");
     }
@@ -878,9 +951,9 @@ int dsmem_hist_partials(const int32_t* keys, int64_t n, int32_t num_bins,
   return run_partials(keys, n, num_bins, plan, partials, accumulate, stream);
 }
 
-int dsmem_hist_reduce(const uint32_t* partials, int32_t num_clusters, int64_t partial_stride,
+int dsmem_hist_reduce(const uint32_t* partials, int32_t num_rows, int64_t partial_stride,
                       int32_t num_bins, uint32_t* bins, cudaStream_t stream) {
-  return run_reduce(partials, num_clusters, partial_stride, num_bins, bins, stream);
+  return run_reduce(partials, num_rows, partial_stride, num_bins, bins, stream);
 }
 
 int dsmem_hist_plan_ex(int32_t num_bins, int64_t n, const dsmem_hist_request_t* request,
@@ -940,6 +1013,14 @@ void dsmem_hist_release(void) {
       st->status_slot.clear();
       for (int i = 0; i < kStatusSlots; ++i)
         st->slot_seq[i] = st->slot_bins_since[i] = 0, st->slot_bins[i] = 0;
+    }
+    if (st->helper_stream) {
+      cudaStreamSynchronize(st->helper_stream);
+      cudaStreamDestroy(st->helper_stream);
+      cudaEventDestroy(st->ev_fork);
+      cudaEventDestroy(st->ev_join);
+      st->helper_stream = nullptr;
+      st->ev_fork = st->ev_join = nullptr;
     }
     if (st->copy_stream) {
       cudaStreamDestroy(st->copy_stream);

@@ -308,15 +308,20 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
   // Key stream: warp tiles of 32 vectors (tile t = vectors 32t .. 32t+31),
   // kKpt/4 consecutive tiles per warp per round; tile indices fit 32 bits with room for
   // three rounds on top (the library keeps n below 2^38 for this kernel).
+  // The rounds cover tiles [0, a.cluster_tiles); with a helper (a.queue
+  // non-null) the tiles after them belong to the helper kernel, and this
+  // kernel's CTAs take those the helper has not claimed when their rounds
+  // are done (see the mop-up below).
   constexpr uint32_t kWarps = kShipThreads / 32;
   const uint32_t nwarps = gridDim.x * kWarps;
   const uint32_t gwarp = blockIdx.x * kWarps + warp;
   const uint32_t ntiles = static_cast<uint32_t>(((a.n - a.head) >> 2) >> 5);
+  const uint32_t ctiles = min(ntiles, a.cluster_tiles);
   const int4* vec = reinterpret_cast<const int4*>(a.keys + a.head) + c.lane;
   constexpr int kTiles = kKpt / 4;
   const uint32_t per_round = nwarps * kTiles;
   const uint32_t wtile0 = gwarp * kTiles;  // this warp's first tile of round 0
-  const uint32_t rounds = static_cast<uint32_t>((static_cast<uint64_t>(ntiles) + per_round - 1) / per_round);
+  const uint32_t rounds = static_cast<uint32_t>((static_cast<uint64_t>(ctiles) + per_round - 1) / per_round);
 
   // Ship and apply: warp w serves owner (and sender) w mod P, as member sg of
   // the sng warps that do; lane l of member sg starts at vector 32*sg + l of
@@ -375,11 +380,11 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
 
     int4 cur[kTiles];
     if (rounds > 0) {
-      load_round<kKpt>(cur, vec, ntiles, wtile0, rounds == 1);
+      load_round<kKpt>(cur, vec, ctiles, wtile0, rounds == 1);
       c.cur_lane = cur_lane0;
       c.lim0 = stage0 + c.blk;
       partition_round<kTiles, kPow2, kSkew>(cur, c, hot_keys);
-      if (rounds > 1) load_round<kKpt>(cur, vec, ntiles, wtile0 + per_round, rounds == 2);
+      if (rounds > 1) load_round<kKpt>(cur, vec, ctiles, wtile0 + per_round, rounds == 2);
     }
     __syncthreads();  // round 0 staged
     uint32_t k = 0;  // r % 3
@@ -442,7 +447,7 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
         c.lim0 = stage0 + (b ^ 1u) * buf_bytes + c.blk;
         partition_round<kTiles, kPow2, kSkew>(cur, c, hot_keys);
         if (r + 2 < rounds)
-          load_round<kKpt>(cur, vec, ntiles, wtile0 + (r + 2) * per_round, r + 3 == rounds);
+          load_round<kKpt>(cur, vec, ctiles, wtile0 + (r + 2) * per_round, r + 3 == rounds);
         __syncwarp();  // the warp's staging stores and cursor updates precede the arrival
         if (c.lane == 0) mbar_arrive_local(staged);
       }
@@ -455,6 +460,45 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
         const uint32_t src = src0 + pb * buf_bytes;
         const uint32_t end = src - vofs + 64u * min(ld_shared_u32(hdr_in + 64u * pb), qs);
         for (uint32_t at = src; at < end; at += step) apply_vector(c.slice, ld_shared_v4(at));
+      }
+    }
+
+    if (a.queue != nullptr) {
+      // Mop-up (single-pass launches with a helper): the helper's tiles
+      // [cluster_tiles, ntiles) are claimed kMopTiles at a time from the
+      // counter the helper claims from, and each key goes straight to its
+      // owner (the pages' per-key DSMEM increment).  When the helper keeps
+      // pace this finds the counter spent at the first claim; when it falls
+      // behind (keys whose global atomics serialise), the clusters finish its
+      // share.  Each CTA claims on its own: the closing barrier below waits
+      // for all of them.  Thread 0 keeps the next claim in flight while the
+      // warps count the current one; it goes to slot j % 2 of the header,
+      // which every thread last read before the barrier of iteration j - 1.
+      const uint32_t slot0 = header0 + 224u;
+      const int4* hvec = vec + static_cast<size_t>(a.cluster_tiles) * 32u;
+      if (threadIdx.x == 0) st_shared_u32(slot0, atomicAdd(a.queue, kMopTiles));
+      __syncthreads();
+      uint32_t t0 = ld_shared_u32(slot0);
+      for (uint32_t j = 1; t0 < a.helper_tiles; ++j) {
+        uint32_t next = 0;
+        if (threadIdx.x == 0) next = atomicAdd(a.queue, kMopTiles);
+        const uint32_t t1 = min(t0 + kMopTiles, a.helper_tiles);
+        for (uint32_t t = t0 + warp; t < t1; t += kWarps) {
+          const int4 v = ld_stream_v4(hvec + static_cast<size_t>(t) * 32u);
+          const int32_t keys[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t rel = static_cast<uint32_t>(keys[u]) - c.base;
+            if (rel < c.range) {
+              uint32_t o, loc;
+              owner_local(rel, c, o, loc, kPow2);
+              red_add_cluster(map_rank(c.slice + 4u * loc, o), 1u);
+            }
+          }
+        }
+        if (threadIdx.x == 0) st_shared_u32(slot0 + 4u * (j & 1u), next);
+        __syncthreads();
+        t0 = ld_shared_u32(slot0 + 4u * (j & 1u));
       }
     }
 
@@ -521,6 +565,75 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
       }
     }
     if (pass + 1 < a.passes) __syncthreads();
+  }
+}
+
+// The helper beside a single-pass ship launch, on the SMs its clusters
+// leave idle (clusters of 8 fit only 15 times into this GPU's 152 SMs).  Its
+// warps claim kHelperTiles tiles at a time of the tiles after the clusters'
+// rounds, [cluster_tiles, cluster_tiles + helper_tiles), from the counter
+// the clusters' mop-up claims from (the next claim in flight while the
+// current one is counted), and count each in-range key into the helper's
+// partial row: with a global atomic, the comparison kernel's method
+// ("Distributed Shared Memory", section "When it beats global atomics"),
+// unless the key owns its slot of a direct-mapped cache in shared memory
+// (kHelperSlots slots of a key and a count; a slot belongs to the first key
+// that reaches it).  Frequent keys take their slots early, so a bin holding
+// a large share of the keys is counted in shared memory instead of
+// serialising the L2 on one address; the cache is added to the row at the
+// end.  Exact: every key is counted once, in its slot or in the row.
+__device__ __forceinline__ void helper_count(int32_t key, uint32_t num_bins, uint32_t* tags,
+                                             uint32_t* cnts, uint32_t* row) {
+  const uint32_t k = static_cast<uint32_t>(key);
+  if (k >= num_bins) return;
+  const uint32_t s = (k * 0x9E3779B1u) >> (32 - kHelperSlotsLog2);
+  uint32_t t = *reinterpret_cast<volatile uint32_t*>(tags + s);
+  if (t == kNoKey) {
+    const uint32_t o = atomicCAS(tags + s, kNoKey, k);
+    t = o == kNoKey ? k : o;
+  }
+  if (t == k)
+    atomicAdd(cnts + s, 1u);
+  else
+    red_add_global(row + k, 1u);
+}
+
+__global__ void __launch_bounds__(kHelperThreads, 1) ship_helper_kernel(const ClusterHistArgs a,
+                                                                      uint32_t* row) {
+  extern __shared__ __align__(16) uint32_t hc[];
+  uint32_t* tags = hc;                  // key owning each slot (kNoKey: free)
+  uint32_t* cnts = hc + kHelperSlots;   // its count
+  for (uint32_t i = threadIdx.x; i < kHelperSlots; i += kHelperThreads) {
+    tags[i] = kNoKey;
+    cnts[i] = 0u;
+  }
+  __syncthreads();
+  const uint32_t lane = threadIdx.x & 31u;
+  const int4* hvec = reinterpret_cast<const int4*>(a.keys + a.head) + lane +
+                     static_cast<size_t>(a.cluster_tiles) * 32u;
+  uint32_t mine = 0;
+  if (lane == 0) mine = atomicAdd(a.queue, kHelperTiles);
+  uint32_t t0 = __shfl_sync(kFullMask, mine, 0);
+  while (t0 < a.helper_tiles) {
+    if (lane == 0) mine = atomicAdd(a.queue, kHelperTiles);  // the next claim
+    int4 v[kHelperTiles];
+#pragma unroll
+    for (uint32_t u = 0; u < kHelperTiles; ++u)
+      v[u] = t0 + u < a.helper_tiles ? ld_stream_v4(hvec + static_cast<size_t>(t0 + u) * 32u)
+                                     : make_int4(-1, -1, -1, -1);
+#pragma unroll
+    for (uint32_t u = 0; u < kHelperTiles; ++u) {
+      helper_count(v[u].x, a.num_bins, tags, cnts, row);
+      helper_count(v[u].y, a.num_bins, tags, cnts, row);
+      helper_count(v[u].z, a.num_bins, tags, cnts, row);
+      helper_count(v[u].w, a.num_bins, tags, cnts, row);
+    }
+    t0 = __shfl_sync(kFullMask, mine, 0);
+  }
+  __syncthreads();
+  for (uint32_t i = threadIdx.x; i < kHelperSlots; i += kHelperThreads) {
+    const uint32_t n = cnts[i];
+    if (n != 0u) red_add_global(row + tags[i], n);
   }
 }
 
@@ -612,6 +725,17 @@ cudaError_t launch_cluster_ship(const dsmem_hist_plan_t& plan, const ClusterHist
               : cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, false, false>, args);
   return p2 ? cudaLaunchKernelEx(&cfg, cluster_ship_kernel<4, true, false>, args)
             : cudaLaunchKernelEx(&cfg, cluster_ship_kernel<4, false, false>, args);
+}
+
+cudaError_t prepare_ship_helper() {
+  return cudaFuncSetAttribute(ship_helper_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kHelperSmemBytes);
+}
+
+cudaError_t launch_ship_helper(const ClusterHistArgs& args, uint32_t* row, int ctas,
+                               cudaStream_t stream) {
+  ship_helper_kernel<<<static_cast<unsigned>(ctas), kHelperThreads, kHelperSmemBytes, stream>>>(args, row);
+  return cudaGetLastError();
 }
 
 }  // namespace dsmh

@@ -54,7 +54,39 @@ struct ClusterHistArgs {
   long long wait_cycles;    // bound of one inbox wait (clock64 cycles)
   uint32_t withhold_last;   // test only: senders skip the last round's arrival and stores
   uint32_t hot_bin;         // ship kernel: the plan's hot bin, 0xFFFFFFFF for none
+  // Ship kernel: its rounds cover tiles [0, cluster_tiles) (128 keys each,
+  // after `head`).  With a helper kernel beside it (single pass only),
+  // `queue` (zeroed before both launch) counts the claimed tiles of the
+  // helper's range [cluster_tiles, cluster_tiles + helper_tiles), which the
+  // cluster kernel's CTAs finish after their rounds; null without a helper.
+  uint32_t cluster_tiles;
+  uint32_t helper_tiles;
+  uint32_t* queue;
 };
+
+// The global-atomic helper on the SMs a ship launch leaves idle: tiles per
+// claim, threads per CTA, the direct-mapped cache of frequent keys in its
+// shared memory (slots of a key and a count), and the fewest keys for which
+// a launch takes a helper.
+constexpr uint32_t kHelperTiles = 4;
+constexpr int kHelperThreads = 1024;
+constexpr int kHelperSlotsLog2 = 13;
+constexpr uint32_t kHelperSlots = 1u << kHelperSlotsLog2;
+constexpr int kHelperSmemBytes = 8 << kHelperSlotsLog2;
+constexpr uint32_t kNoKey = 0xFFFFFFFFu;
+constexpr int64_t kHelperMinKeys = int64_t{1} << 24;
+// Fewest idle SMs for which a plan takes the helper.
+constexpr int64_t kHelperMinIdleSms = 4;
+
+// A plan's partial rows (one per cluster, plus the helper's) and its
+// scratch: the rows, then (with the helper) 16 bytes of tile counter.
+inline void set_partial_rows(dsmem_hist_plan_t* p, bool helper) {
+  p->partial_rows = p->num_clusters + (helper ? 1 : 0);
+  p->workspace_bytes = static_cast<int64_t>(p->partial_rows) * p->partial_stride * 4 + (helper ? 16 : 0);
+}
+
+// Tiles per claim of the ship kernel's mop-up: two per warp.
+constexpr uint32_t kMopTiles = 2 * (kShipThreads / 32);
 
 // Streams per device with their own status words (later streams share the
 // last slot).
@@ -74,6 +106,12 @@ cudaError_t launch_reduce_partials(const uint32_t* partials, uint64_t stride,
                                    cudaStream_t stream, uint32_t hot_min = 0,
                                    unsigned long long* hot_word = nullptr,
                                    uint32_t* seq_word = nullptr, uint32_t seq = 0);
+// The helper: `ctas` CTAs of kHelperThreads threads and kHelperSmemBytes of
+// shared memory (prepare_ship_helper sets the limit once per device) count
+// the tiles of args' helper range they claim from args.queue into `row`.
+cudaError_t prepare_ship_helper();
+cudaError_t launch_ship_helper(const ClusterHistArgs& args, uint32_t* row, int ctas,
+                               cudaStream_t stream);
 cudaError_t launch_global_atomic(const int32_t* keys, int64_t n, uint32_t num_bins,
                                  uint32_t* bins, cudaStream_t stream);
 // Work-free control kernel with a plan's grid, cluster and shared memory.

@@ -25,6 +25,10 @@
 //             least kMinShipRoundsPerCta rounds (SHIP) or kMinStepsPerCta
 //             unrolled steps (DIRECT) of keys, clusters whose partial rows
 //             fit kMaxAutoScratchBytes), at least 1
+//   helper  = one more partial row, for the global-atomic helper kernel on
+//             the SMs the clusters leave idle, when the plan is a
+//             single-pass SHIP plan of at least kHelperMinKeys keys without
+//             a hot bin and at least kHelperMinIdleSms SMs stay idle
 #include <stdint.h>
 
 #include "internal.h"
@@ -216,7 +220,10 @@ int plan_shape(const dsmem_hist_device_t* dev, int32_t num_bins, int64_t n,
     out->hot_bin = req->hot_bin;
   }
   out->partial_stride = stride;
-  out->workspace_bytes = C * stride * 4;
+  const int64_t idle = static_cast<int64_t>(dev->sm_count) - C * P;
+  const bool helper = kernel == DSMEM_HIST_KERNEL_SHIP && passes == 1 && n >= kHelperMinKeys &&
+                      out->hot_bin < 0 && idle >= kHelperMinIdleSms;
+  set_partial_rows(out, helper);
   return DSMEM_HIST_OK;
 }
 

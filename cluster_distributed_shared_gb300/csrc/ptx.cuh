@@ -110,6 +110,9 @@ __device__ __forceinline__ uint32_t map_rank(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void red_add_cluster(uint32_t cluster_addr, uint32_t v) {
   asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v));
 }
+__device__ __forceinline__ void red_add_global(uint32_t* p, uint32_t v) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ void red_add_local(uint32_t cta_addr, uint32_t v) {
   asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(cta_addr), "r"(v));
 }

@@ -112,8 +112,13 @@ typedef struct dsmem_hist_plan {
                                   its keys are counted in registers instead of staged (see
                                   dsmem_hist_request_t.hot_bin).  -1: none.  The planner sets it
                                   only on request; dsmem_hist_partials uses it as given */
-  int64_t partial_stride;      /* u32 elements between two clusters' partial rows (num_bins rounded up to 4) */
-  int64_t workspace_bytes;     /* scratch: num_clusters * partial_stride * 4 */
+  int32_t partial_rows;        /* partial rows the reduction sums: num_clusters, plus one when a
+                                  helper kernel runs beside a single-pass ship launch of at least
+                                  2^24 keys without a hot bin, on the SMs its clusters leave idle
+                                  (see dsmem_hist_partials) */
+  int64_t partial_stride;      /* u32 elements between two partial rows (num_bins rounded up to 4) */
+  int64_t workspace_bytes;     /* scratch: partial_rows * partial_stride * 4, plus 16 bytes of
+                                  tile counter with the helper */
 } dsmem_hist_plan_t;
 
 /* Planner overrides; a zero field (or -1 for `aggregate` and `kernel`) means "choose". */
@@ -193,29 +198,41 @@ DSMEM_HIST_API int dsmem_hist_global_atomic(const int32_t* keys, int64_t n, int3
 DSMEM_HIST_API int dsmem_hist_host(const int32_t* h_keys, int64_t n, int32_t num_bins, uint32_t* h_bins,
                     cudaStream_t stream);
 
-/* Stage 1 of dsmem_hist, with caller-owned scratch: every cluster of `plan`
- * writes (accumulate == 0) or adds into (accumulate == 1) its partial row
- *     partials[c * plan->partial_stride + b],  c < plan->num_clusters,
- * which, summed over c, is the histogram of these keys ("Distributed Shared
+/* Stage 1 of dsmem_hist, with caller-owned scratch: the plan's kernels write
+ * (accumulate == 0) or add into (accumulate == 1) the partial rows
+ *     partials[r * plan->partial_stride + b],  r < plan->partial_rows,
+ * which, summed over r, are the histogram of these keys ("Distributed Shared
  * Memory", section "The cluster histogram": zero, barrier, DSMEM increments,
- * barrier, flush).
+ * barrier, flush).  Row c < num_clusters is cluster c's.  With a helper row
+ * (partial_rows == num_clusters + 1: a single-pass ship plan of at least
+ * 2^24 keys, no hot bin, and SMs left idle by the clusters) a global-atomic
+ * helper kernel runs beside the clusters on the idle SMs, on a second
+ * stream of the library forked from and joined back into `stream`: the
+ * clusters' rounds take the first tiles of the keys, the helper the rest
+ * ("When it beats global atomics": one global atomic per key, into the last
+ * row), and clusters that finish early take the helper's tiles it has not
+ * claimed yet.  DSMEM_HIST_HELPER=0 in the environment makes the planner
+ * leave the helper out.
  *   plan      from dsmem_hist_plan for the same num_bins (checked for
  *             consistency; EINVAL otherwise)
- *   partials  device, 16-byte aligned, num_clusters * partial_stride uint32;
- *             with accumulate == 1 it must hold the rows of an earlier call
- *             with the same plan (used to fold key chunks into one histogram)
+ *   partials  device, 16-byte aligned, plan->workspace_bytes bytes: the
+ *             partial rows, then (helper) a tile counter the call zeroes;
+ *             with accumulate == 1 the rows must hold those of an earlier
+ *             call with the same plan (used to fold key chunks into one
+ *             histogram)
  * Asynchronous on `stream`. */
 DSMEM_HIST_API int dsmem_hist_partials(const int32_t* keys, int64_t n, int32_t num_bins,
                                        const dsmem_hist_plan_t* plan, uint32_t* partials,
                                        int32_t accumulate, cudaStream_t stream);
 
-/* Stage 2 of dsmem_hist: bins[b] = sum over c < num_clusters of
- * partials[c * partial_stride + b] (mod 2^32), b < num_bins.
+/* Stage 2 of dsmem_hist: bins[b] = sum over r < num_rows of
+ * partials[r * partial_stride + b] (mod 2^32), b < num_bins.
  *   partials  device, 16-byte aligned; partial_stride a multiple of 4 and
  *             >= num_bins
+ *   num_rows  rows to sum: the plan's partial_rows after dsmem_hist_partials
  *   bins      device, num_bins uint32 (overwritten)
  * Asynchronous on `stream`. */
-DSMEM_HIST_API int dsmem_hist_reduce(const uint32_t* partials, int32_t num_clusters,
+DSMEM_HIST_API int dsmem_hist_reduce(const uint32_t* partials, int32_t num_rows,
                                      int64_t partial_stride, int32_t num_bins, uint32_t* bins,
                                      cudaStream_t stream);
 

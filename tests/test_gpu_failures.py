@@ -96,7 +96,7 @@ def test_partials_entry_reports_a_timeout_of_an_earlier_launch(monkeypatch):
     keys_np = gen.uniform(n, num_bins, seed=72)
     keys = torch.from_numpy(keys_np).cuda()
     plan = pkg.dsmem_hist_plan(num_bins, n, cluster_size=2, kernel=pkg.KERNEL_SHIP)
-    partials = torch.empty(plan["num_clusters"] * plan["partial_stride"], dtype=torch.int32,
+    partials = torch.empty(-(-plan["workspace_bytes"] // 4), dtype=torch.int32,
                            device="cuda")
     s = torch.cuda.Stream()
     monkeypatch.setenv("DSMEM_HIST_TEST_WITHHOLD_LAST_ROUND", "1")
@@ -109,7 +109,7 @@ def test_partials_entry_reports_a_timeout_of_an_earlier_launch(monkeypatch):
         pkg.dsmem_hist_partials(keys, num_bins, plan, partials, 0, s)
     assert e.value.code == pkg.DSMEM_HIST_ETIMEOUT
     pkg.dsmem_hist_partials(keys, num_bins, plan, partials, 0, s)
-    bins = pkg.dsmem_hist_reduce(partials, plan["num_clusters"], plan["partial_stride"],
+    bins = pkg.dsmem_hist_reduce(partials, plan["partial_rows"], plan["partial_stride"],
                                  num_bins, stream=s)
     s.synchronize()
     assert np.array_equal(_bits(bins), oracle.histogram(keys_np, num_bins))

@@ -342,11 +342,12 @@ def test_long_round_chains_in_one_cluster(P, kpt):
     plan["keys_per_thread"] = kpt
     rounds = n // (P * pkg.SHIP_THREADS * kpt)
     assert plan["num_clusters"] == 1 and plan["bins_per_cta"] == 32768 and rounds >= 70
-    partials = torch.empty(plan["partial_stride"], dtype=torch.int32, device="cuda")
+    partials = torch.empty(-(-plan["workspace_bytes"] // 4), dtype=torch.int32, device="cuda")
     s = torch.cuda.current_stream()
     for _ in range(3):
         pkg.dsmem_hist_partials(keys, num_bins, plan, partials, 0, s)
-        bins = pkg.dsmem_hist_reduce(partials, 1, plan["partial_stride"], num_bins, stream=s)
+        bins = pkg.dsmem_hist_reduce(partials, plan["partial_rows"], plan["partial_stride"], num_bins,
+                                     stream=s)
         torch.cuda.synchronize()
         assert np.array_equal(to_np(bins), want)
     assert pkg.dsmem_hist_device_status() == 0
@@ -442,10 +443,10 @@ def test_hot_bin_hint_is_exact(share):
     plan = pkg.dsmem_hist_plan(num_bins, n, cluster_size=2, hot_bin=hb)
     assert plan["hot_bin"] == hb and plan["passes"] == 4   # the hot bin lies in one of four passes
     # through the two-stage entry points with the hinted plan
-    partials = torch.empty(plan["num_clusters"] * plan["partial_stride"], dtype=torch.int32,
+    partials = torch.empty(-(-plan["workspace_bytes"] // 4), dtype=torch.int32,
                            device="cuda")
     pkg.dsmem_hist_partials(d, num_bins, plan, partials)
-    got = to_np(pkg.dsmem_hist_reduce(partials, plan["num_clusters"], plan["partial_stride"],
+    got = to_np(pkg.dsmem_hist_reduce(partials, plan["partial_rows"], plan["partial_stride"],
                                       num_bins))
     torch.cuda.synchronize()
     assert np.array_equal(got, want)
@@ -524,3 +525,46 @@ def test_hot_bin_kernel_is_chosen_from_the_previous_histogram():
     assert chose["uni2"] is None                        # uniform keys report no hot bin
     assert chose["hot4"] is None and chose["hot5"] == hot_bin
     assert chose["off"] is None
+
+
+@pytest.mark.parametrize("mode,share", [("0", None), ("1", None), ("1", "0"), ("1", "0.5"),
+                                        ("1", "1")])
+def test_idle_sm_helper_and_mop_up(monkeypatch, mode, share):
+    """Clusters of 8 leave 32 SMs idle; a global-atomic helper kernel on them
+    takes the tiles after the clusters' rounds, and clusters that finish
+    early take the ones it has not claimed.  Exact with the helper off, at
+    its planned share, with no tiles for it, with half and with all of them
+    (the clusters' mop-up then does much of the work): on uniform, Zipf and
+    run-heavy keys, at a pointer offset, through the product call, the
+    two-stage entry points (accumulating too) and the host entry point."""
+    monkeypatch.setenv("DSMEM_HIST_HELPER", mode)
+    if share is not None:
+        monkeypatch.setenv("DSMEM_HIST_HELPER_SHARE", share)
+    num_bins = 262144
+    n = (1 << 25) + 1001
+    cases = [gen.uniform(n, num_bins, seed=81), gen.zipf(n, num_bins, seed=82),
+             gen.workload("runs256-1G-512K", 83, n=1 << 25) % num_bins]
+    for keys in cases:
+        keys = np.ascontiguousarray(keys, np.int32)
+        want = oracle.histogram(keys, num_bins)
+        assert np.array_equal(gpu_hist(keys, num_bins, cluster_size=8), want)
+        d = torch.from_numpy(keys).cuda()
+        sub = d[3:]                                          # 12-byte offset: a scalar head
+        want_sub = oracle.histogram(keys[3:], num_bins)
+        out = torch.empty(num_bins, dtype=torch.int32, device="cuda")
+        pkg.dsmem_hist(sub, num_bins, out=out, cluster_size=8)
+        torch.cuda.synchronize()
+        assert np.array_equal(to_np(out), want_sub)
+        plan = pkg.dsmem_hist_plan(num_bins, sub.numel(), cluster_size=8)
+        assert plan["kernel"] == SH and plan["passes"] == 1
+        assert plan["partial_rows"] == plan["num_clusters"] + (mode != "0")
+        partials = torch.empty(-(-plan["workspace_bytes"] // 4), dtype=torch.int32, device="cuda")
+        half = (sub.numel() // 2) & ~127
+        pkg.dsmem_hist_partials(sub[:half], num_bins, plan, partials, 0)
+        pkg.dsmem_hist_partials(sub[half:], num_bins, plan, partials, 1)
+        got = to_np(pkg.dsmem_hist_reduce(partials, plan["partial_rows"], plan["partial_stride"],
+                                          num_bins, out))
+        assert np.array_equal(got, want_sub)
+        assert np.array_equal(pkg.dsmem_hist_host(keys, num_bins), want)
+        del d, sub
+    assert pkg.dsmem_hist_device_status() == 0
