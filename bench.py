@@ -217,10 +217,11 @@ def kernel_sources_sha256(kernel_id):
 
 
 def kernel_traffic(workload, n_keys, num_bins, cluster_size, kernel_id, block_threads):
-    """Per-launch DRAM bytes of the cluster kernel from the committed ncu
-    summary of the same workload, scaled to this launch's keys; None when no
-    capture of that workload and shape exists or the kernel's sources or its
-    block size have changed since the counters were taken."""
+    """DRAM bytes of one partials stage (the cluster kernel, plus the idle-SM
+    helper where the capture has one) from the committed ncu summary of the
+    same workload, scaled to this launch's keys; None when no capture of that
+    workload and shape exists or the kernels' sources or the block size have
+    changed since the counters were taken."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
@@ -490,6 +491,7 @@ def run_ours(a, world, rank, local):
     alg_bytes = 4 * n + 4 * num_bins
     achieved = alg_bytes / (cluster_ms / 1e3) / 1e9
     traffic = kernel_traffic(cfg["workload"], n, num_bins, P, plan["kernel"], plan["block_threads"])
+    helper = plan["partial_rows"] > plan["num_clusters"]
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -498,7 +500,11 @@ def run_ours(a, world, rank, local):
         "plan": plan,
         "achieved_gbs": world * alg_bytes / (ms_step / 1e3) / 1e9,
         "pct_of_nominal_8tbs": 100.0 * (alg_bytes / (ms_step / 1e3) / 1e9) / NOMINAL_HBM_GBS,
-        "roofline": {"bound": "hbm", "kernel": KERNEL_SOURCES[plan["kernel"]][0], "achieved": achieved,
+        "roofline": {"bound": "hbm", "kernel": KERNEL_SOURCES[plan["kernel"]][0],
+                     "stage": ("partials stage: the cluster kernel and, on the SMs its clusters "
+                               "leave idle, the helper kernel (second stream, forked and joined)"
+                               if helper else "partials stage: the cluster kernel"),
+                     "achieved": achieved,
                      "peak": peak, "peak_source": peak_src, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes": alg_bytes, "avg_launch_ms": cluster_ms,
@@ -507,7 +513,8 @@ def run_ours(a, world, rank, local):
         "e2e": e2e,
         "product_call": product_call,
         "global_atomic_comparison": comparison,
-        "gpu_launches": 2 * a.steps,  # timed region: one cluster kernel + one reduction per step
+        # timed region, per step: the cluster kernel, the helper (if planned), the reduction
+        "gpu_launches": (3 if helper else 2) * a.steps,
         "clocks": clocks,
         "parity": parity,
     }
