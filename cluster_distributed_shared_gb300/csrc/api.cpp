@@ -62,6 +62,12 @@ struct DeviceState {
   cudaStream_t helper_stream = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   std::mutex helper_call;
+  // Per stream slot, under helper_call: the helper's current share of the
+  // tiles (0: none learned yet), the last report taken, and the last
+  // sequence number handed out.
+  double helper_share[kStatusSlots] = {};
+  uint32_t helper_taken[kStatusSlots] = {};
+  uint32_t helper_seq[kStatusSlots] = {};
   // Per-stream words in pinned, host-mapped memory (h_status on the host,
   // d_status the same memory for the device), kStatusSlots of each kind: the
   // ship kernel's u32 status words; u32 sequence stamps, the number of the
@@ -80,7 +86,7 @@ struct DeviceState {
 };
 
 // Bytes of the host-mapped block: status words, sequence stamps, hot-bin words.
-constexpr size_t kMappedBytes = kStatusSlots * (2 * sizeof(uint32_t) + sizeof(unsigned long long));
+constexpr size_t kMappedBytes = kStatusSlots * (2 * sizeof(uint32_t) + 2 * sizeof(unsigned long long));
 // The hot-bin kernel is chosen when one bin held at least 1/kHotShareDen of
 // the keys of the previous histogram on the same stream.
 constexpr int64_t kHotShareDen = 6;
@@ -94,6 +100,8 @@ struct SlotRef {
   uint32_t* d_seq = nullptr;
   unsigned long long* h_hot = nullptr;
   unsigned long long* d_hot = nullptr;
+  unsigned long long* h_helper = nullptr;  // the helper's progress report
+  unsigned long long* d_helper = nullptr;
 };
 
 // What the reduction of a histogram reports for later calls on its stream.
@@ -197,6 +205,8 @@ int stream_slot(DeviceState* st, cudaStream_t stream, bool may_alloc, SlotRef* r
   r->d_seq = st->d_status + kStatusSlots + slot;
   r->h_hot = reinterpret_cast<unsigned long long*>(st->h_status + 2 * kStatusSlots) + slot;
   r->d_hot = reinterpret_cast<unsigned long long*>(st->d_status + 2 * kStatusSlots) + slot;
+  r->h_helper = reinterpret_cast<unsigned long long*>(st->h_status + 4 * kStatusSlots) + slot;
+  r->d_helper = reinterpret_cast<unsigned long long*>(st->d_status + 4 * kStatusSlots) + slot;
   return DSMEM_HIST_OK;
 }
 
@@ -241,7 +251,6 @@ int32_t choose_hot_bin(DeviceState* st, const SlotRef& r, int64_t n, int32_t num
 void use_hot_bin(dsmem_hist_plan_t* plan, int32_t chosen, const SlotRef& r) {
   if (chosen < 0 || plan->kernel != DSMEM_HIST_KERNEL_SHIP) return;
   plan->hot_bin = chosen;
-  set_partial_rows(plan, false);  // a hot bin would serialise the helper's atomics
   if (trace_enabled())
     fprintf(stderr, "[dsmem_hist] stream slot %d: bin %d held a sixth or more of the keys of a "
             "recent histogram -> hot-bin kernel\n", r.slot, chosen);
@@ -297,20 +306,51 @@ int prepare_locked(DeviceState* st, const dsmem_hist_plan_t& p) {
 }
 
 // The helper's speed per idle SM relative to a cluster SM's (global atomics
-// against the ship kernel, measured on uniform keys: about 1.5 against 4.3
-// G keys/s per SM); it sets the helper's share of the tiles.
-constexpr double kHelperRelativeRate = 0.35;
+// against the ship kernel, measured on uniform keys); it sets the helper's
+// share of the tiles until a stream has reported how the split went.
+constexpr double kHelperRelativeRate = 0.42;
+constexpr double kHelperShareMin = 0.01, kHelperShareMax = 0.6;
+
+// The helper's share for the next launch on the stream of `sr`: the share it
+// has learned, else `prior`.  Each launch with a helper reports, from the
+// first CTA done with its rounds, the share at which the helper and the
+// clusters would have finished together (report_helper_share in the ship
+// kernel); a new report moves the share three quarters of the way to it.
+// st->helper_call must be held.
+double helper_share(DeviceState* st, const SlotRef* sr, double prior) {
+  if (!sr || sr->slot < 0 || !sr->h_helper) return prior;
+  const int slot = sr->slot;
+  double& share = st->helper_share[slot];
+  if (share <= 0.0) share = prior;
+  const unsigned long long w = *reinterpret_cast<volatile unsigned long long*>(sr->h_helper);
+  const uint32_t seq = static_cast<uint32_t>(w >> 32), bits = static_cast<uint32_t>(w);
+  if (seq != 0 && seq != st->helper_taken[slot]) {
+    st->helper_taken[slot] = seq;
+    float target = 0.0f;
+    memcpy(&target, &bits, sizeof target);
+    if (target > 0.0f && target < 1.0f) {
+      const double before = share;
+      share = 0.25 * share + 0.75 * target;
+      share = share < kHelperShareMin ? kHelperShareMin : (share > kHelperShareMax ? kHelperShareMax : share);
+      if (trace_enabled())
+        fprintf(stderr, "[dsmem_hist] stream slot %d: helper launch %u reports share %.4f -> share "
+                "%.4f -> %.4f\n", slot, seq, target, before, share);
+    }
+  }
+  return share;
+}
 
 // Launches a plan.  With `st` non-null and a helper row in the plan
 // (partial_rows > num_clusters), the ship kernel's rounds cover the first
 // tiles and the global-atomic helper, on the SMs the clusters leave idle,
-// takes the rest: its share is what the idle SMs would finish in the time
-// the clusters take for theirs, and the clusters' rounds are rounded down
-// to whole rounds.  The helper runs on a second stream forked from and
-// joined back into `stream`; the tile counter is zeroed on `stream` before
-// the fork and the helper's row on the helper stream (unless accumulating).
+// takes the rest: its share starts at what the idle SMs would finish in the
+// time the clusters take for theirs and then follows the stream's reports
+// (helper_share); the clusters' rounds are rounded down to whole rounds.
+// The helper runs on a second stream forked from and joined back into
+// `stream`; the tile counter is zeroed on `stream` before the fork and the
+// helper's row on the helper stream (unless accumulating).
 cudaError_t launch_plan(const dsmem_hist_plan_t& plan, ClusterHistArgs args, cudaStream_t stream,
-                        DeviceState* st = nullptr) {
+                        DeviceState* st = nullptr, const SlotRef* sr = nullptr) {
   if (plan.kernel != DSMEM_HIST_KERNEL_SHIP) return launch_cluster_hist(plan, args, stream);
   const uint32_t ntiles = static_cast<uint32_t>(((args.n - args.head) >> 2) >> 5);
   args.cluster_tiles = ntiles;
@@ -331,7 +371,7 @@ cudaError_t launch_plan(const dsmem_hist_plan_t& plan, ClusterHistArgs args, cud
   }
   const int active = plan.num_clusters * plan.cluster_size;
   const int idle = st->dev.sm_count > active ? st->dev.sm_count - active : 0;
-  double share = idle * kHelperRelativeRate / (active + idle * kHelperRelativeRate);
+  double share = helper_share(st, sr, idle * kHelperRelativeRate / (active + idle * kHelperRelativeRate));
   if (const char* v = getenv("DSMEM_HIST_HELPER_SHARE")) share = atof(v);  // sweeps
   share = share < 0.0 ? 0.0 : (share > 1.0 ? 1.0 : share);
   const uint64_t per_round = static_cast<uint64_t>(active) * (kShipThreads / 32) * (plan.keys_per_thread / 4);
@@ -340,10 +380,19 @@ cudaError_t launch_plan(const dsmem_hist_plan_t& plan, ClusterHistArgs args, cud
   args.helper_tiles = ntiles - args.cluster_tiles;
   uint32_t* row = args.partials + static_cast<size_t>(plan.num_clusters) * args.stride;
   args.queue = args.partials + static_cast<size_t>(plan.partial_rows) * args.stride;
+  if (sr && sr->slot >= 0 && sr->d_helper) {
+    // A new sequence number tells this launch's report from older ones.
+    const int slot = sr->slot;
+    uint32_t seq = st->helper_seq[slot] + 1;
+    if (seq == 0) seq = 1;
+    st->helper_seq[slot] = seq;
+    args.helper_report = sr->d_helper;
+    args.helper_seq = seq;
+  }
   // The clusters are launched first, so they take their SMs before the
   // helper's CTAs fill the idle ones; a cluster that still finds no room
   // starts later, and the mop-up balances the work either way.
-  if ((e = cudaMemsetAsync(args.queue, 0, 16, stream)) != cudaSuccess ||
+  if ((e = cudaMemsetAsync(args.queue, 0, kHelperQueueBytes, stream)) != cudaSuccess ||
       (e = cudaEventRecord(st->ev_fork, stream)) != cudaSuccess ||
       (e = cudaStreamWaitEvent(st->helper_stream, st->ev_fork, 0)) != cudaSuccess ||
       (!args.accumulate &&
@@ -485,6 +534,8 @@ ClusterHistArgs make_args(const dsmem_hist_plan_t& plan, const int32_t* keys, in
   a.cluster_tiles = 0xFFFFFFFFu;  // launch_plan sets the helper's split
   a.helper_tiles = 0;
   a.queue = nullptr;
+  a.helper_report = nullptr;
+  a.helper_seq = 0;
   return a;
 }
 
@@ -526,7 +577,7 @@ int run_device(const int32_t* keys, int64_t n, int32_t num_bins, uint32_t* bins,
   uint32_t* partials = static_cast<uint32_t*>(scratch);
   ClusterHistArgs args = make_args(plan, keys, n, num_bins, partials, 0);
   args.status = sr.d_status;
-  e = launch_plan(plan, args, stream, st);
+  e = launch_plan(plan, args, stream, st, &sr);
   if (e == cudaSuccess)
     e = launch_reduce_partials(partials, args.stride, static_cast<uint32_t>(plan.partial_rows),
                                args.num_bins, bins, stream, hot_report.min_count,
@@ -568,10 +619,9 @@ int check_plan(const DeviceState* st, const dsmem_hist_plan_t* p, int32_t num_bi
       (p->hot_bin >= 0 && p->kernel != DSMEM_HIST_KERNEL_SHIP))
     return fail(DSMEM_HIST_EINVAL, "plan: hot_bin must be -1 or a bin of a ship-kernel plan");
   if (p->partial_rows != p->num_clusters &&
-      !(p->partial_rows == p->num_clusters + 1 && p->kernel == DSMEM_HIST_KERNEL_SHIP &&
-        p->passes == 1 && p->hot_bin < 0))
+      !(p->partial_rows == p->num_clusters + 1 && p->kernel == DSMEM_HIST_KERNEL_SHIP && p->passes == 1))
     return fail(DSMEM_HIST_EINVAL, "plan: partial_rows must be num_clusters, or num_clusters + 1 "
-                "(the helper's row) for a single-pass ship plan without a hot bin");
+                "(the helper's row) for a single-pass ship plan");
   return DSMEM_HIST_OK;
 }
 
@@ -597,7 +647,7 @@ int run_partials(const int32_t* keys, int64_t n, int32_t num_bins, const dsmem_h
   // The caller's plan decides the kernel (its hot_bin included): no automatic choice.
   ClusterHistArgs args = make_args(*plan, keys, n, num_bins, partials, accumulate);
   args.status = sr.d_status;
-  const cudaError_t e = launch_plan(*plan, args, stream, st);
+  const cudaError_t e = launch_plan(*plan, args, stream, st, &sr);
   return e == cudaSuccess ? DSMEM_HIST_OK : fail_cuda(e, "cluster histogram launch");
 }
 
@@ -690,7 +740,7 @@ int run_host(const int32_t* h_keys, int64_t n, int32_t num_bins, uint32_t* h_bin
     }
     ClusterHistArgs args = make_args(plan, stage[b], cnt, num_bins, partials, j > 0);
     args.status = sr.d_status;
-    if ((e = launch_plan(plan, args, stream, st)) != cudaSuccess ||
+    if ((e = launch_plan(plan, args, stream, st, &sr)) != cudaSuccess ||
         (e = cudaEventRecord(st->ev_consumed[b], stream)) != cudaSuccess) {
       rc = fail_cuda(e, "cluster histogram launch");
       break;

@@ -247,6 +247,26 @@ __device__ __forceinline__ uint4 pad_vector(uint32_t pad0) {
   return make_uint4(pad0, pad0 + 0x00020002u, pad0 + 0x00040004u, pad0 + 0x00060006u);
 }
 
+// Reports, from the first CTA whose rounds are done, the helper's share of
+// the tiles at which the helper and the clusters would have finished
+// together.  rho is how far the helper's pace carried it through its range
+// by now: the ratio of the times since the launch started when the helper
+// kernel has finished already, else the fraction of its tiles claimed.
+// With helper share f the target is rho f / (rho f + 1 - f).
+__device__ __noinline__ void report_helper_share(const ClusterHistArgs& a, uint32_t claimed) {
+  const unsigned long long* times = reinterpret_cast<const unsigned long long*>(a.queue + 2);
+  const unsigned long long now = global_timer_ns();
+  const unsigned long long t0 = ld_volatile_u64(times), th = ld_volatile_u64(times + 1);
+  if (a.helper_tiles == 0 || a.cluster_tiles == 0 || t0 == 0 || now <= t0) return;
+  const float H = static_cast<float>(a.helper_tiles), C = static_cast<float>(a.cluster_tiles);
+  const float rho = th > t0 && th <= now ? static_cast<float>(now - t0) / static_cast<float>(th - t0)
+                                         : fminf(static_cast<float>(claimed), H) / H;
+  const float f = H / (H + C);
+  const float target = rho * f / (rho * f + 1.0f - f);
+  st_volatile_u64(a.helper_report,
+                  (static_cast<unsigned long long>(a.helper_seq) << 32) | __float_as_uint(target));
+}
+
 // Loads a warp's consecutive tiles t0, t0 + 1, ... of a round; tiles past
 // the end read as keys -1 (outside every pass).  Only the last round can
 // reach past the end.
@@ -369,6 +389,8 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
     }
     if (threadIdx.x < 32u) st_shared_u32(header0 + 4u * threadIdx.x, 0u);
     if (threadIdx.x == 0) st_shared_u32(gave_up, 0u);
+    if (a.queue != nullptr && pass == 0 && rank == 0 && threadIdx.x == 0)
+      atomicCAS(reinterpret_cast<unsigned long long*>(a.queue + 2), 0ull, global_timer_ns());
     if (threadIdx.x == 0) {
       // One arrival per other sender and round; their bytes complete it.
       mbar_init(full0, P - 1u);
@@ -476,7 +498,13 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
       // which every thread last read before the barrier of iteration j - 1.
       const uint32_t slot0 = header0 + 224u;
       const int4* hvec = vec + static_cast<size_t>(a.cluster_tiles) * 32u;
-      if (threadIdx.x == 0) st_shared_u32(slot0, atomicAdd(a.queue, kMopTiles));
+      if (threadIdx.x == 0) {
+        const uint32_t first = atomicAdd(a.queue, kMopTiles);
+        st_shared_u32(slot0, first);
+        // The first CTA done with its rounds reports how the split went.
+        if (a.helper_report != nullptr && atomicCAS(a.queue + 1, 0u, 1u) == 0u)
+          report_helper_share(a, first);
+      }
       __syncthreads();
       uint32_t t0 = ld_shared_u32(slot0);
       for (uint32_t j = 1; t0 < a.helper_tiles; ++j) {
@@ -581,7 +609,8 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
 // that reaches it).  Frequent keys take their slots early, so a bin holding
 // a large share of the keys is counted in shared memory instead of
 // serialising the L2 on one address; the cache is added to the row at the
-// end.  Exact: every key is counted once, in its slot or in the row.
+// end.  A tile of 128 equal keys (runs) is one atomic of 128.  Exact: every
+// key is counted once, in its slot or in the row.
 __device__ __forceinline__ void helper_count(int32_t key, uint32_t num_bins, uint32_t* tags,
                                              uint32_t* cnts, uint32_t* row) {
   const uint32_t k = static_cast<uint32_t>(key);
@@ -623,6 +652,13 @@ __global__ void __launch_bounds__(kHelperThreads, 1) ship_helper_kernel(const Cl
                                      : make_int4(-1, -1, -1, -1);
 #pragma unroll
     for (uint32_t u = 0; u < kHelperTiles; ++u) {
+      // A tile of 128 equal keys (runs) is one atomic of 128.
+      const int32_t k0 = __shfl_sync(kFullMask, v[u].x, 0);
+      const bool eq = (v[u].x == k0) & (v[u].y == k0) & (v[u].z == k0) & (v[u].w == k0);
+      if (__all_sync(kFullMask, eq)) {
+        if (lane == 0 && static_cast<uint32_t>(k0) < a.num_bins) red_add_global(row + k0, 128u);
+        continue;
+      }
       helper_count(v[u].x, a.num_bins, tags, cnts, row);
       helper_count(v[u].y, a.num_bins, tags, cnts, row);
       helper_count(v[u].z, a.num_bins, tags, cnts, row);
@@ -635,6 +671,11 @@ __global__ void __launch_bounds__(kHelperThreads, 1) ship_helper_kernel(const Cl
     const uint32_t n = cnts[i];
     if (n != 0u) red_add_global(row + tags[i], n);
   }
+  // The last CTA to finish stamps the time (for the report in the cluster
+  // kernel's mop-up).
+  __syncthreads();
+  if (threadIdx.x == 0 && atomicAdd(a.queue + 6, 1u) == gridDim.x - 1u)
+    atomicExch(reinterpret_cast<unsigned long long*>(a.queue + 4), global_timer_ns());
 }
 
 template <int kKpt, bool kPow2, bool kSkew>

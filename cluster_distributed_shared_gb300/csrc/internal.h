@@ -62,7 +62,17 @@ struct ClusterHistArgs {
   uint32_t cluster_tiles;
   uint32_t helper_tiles;
   uint32_t* queue;
+  // With a helper: the first of this launch's CTAs to finish its rounds
+  // writes (helper_seq << 32) | (bits of a float: the helper's share at which
+  // both sides would have finished together) to this pinned, host-mapped
+  // word (may be null), from which the next launch on the stream sets the
+  // helper's share.  The zeroed kHelperQueueBytes at `queue`: u32 tile
+  // counter, u32 report flag, u64 globaltimer of the cluster kernel's start,
+  // u64 globaltimer of the helper kernel's end, u32 helper CTAs finished.
+  unsigned long long* helper_report;
+  uint32_t helper_seq;
 };
+constexpr int64_t kHelperQueueBytes = 32;
 
 // The global-atomic helper on the SMs a ship launch leaves idle: tiles per
 // claim, threads per CTA, the direct-mapped cache of frequent keys in its
@@ -79,10 +89,12 @@ constexpr int64_t kHelperMinKeys = int64_t{1} << 24;
 constexpr int64_t kHelperMinIdleSms = 4;
 
 // A plan's partial rows (one per cluster, plus the helper's) and its
-// scratch: the rows, then (with the helper) 16 bytes of tile counter.
+// scratch: the rows, then (with the helper) kHelperQueueBytes of tile
+// counter and timing.
 inline void set_partial_rows(dsmem_hist_plan_t* p, bool helper) {
   p->partial_rows = p->num_clusters + (helper ? 1 : 0);
-  p->workspace_bytes = static_cast<int64_t>(p->partial_rows) * p->partial_stride * 4 + (helper ? 16 : 0);
+  p->workspace_bytes = static_cast<int64_t>(p->partial_rows) * p->partial_stride * 4 +
+                       (helper ? kHelperQueueBytes : 0);
 }
 
 // Tiles per claim of the ship kernel's mop-up: two per warp.

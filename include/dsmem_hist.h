@@ -114,11 +114,11 @@ typedef struct dsmem_hist_plan {
                                   only on request; dsmem_hist_partials uses it as given */
   int32_t partial_rows;        /* partial rows the reduction sums: num_clusters, plus one when a
                                   helper kernel runs beside a single-pass ship launch of at least
-                                  2^24 keys without a hot bin, on the SMs its clusters leave idle
-                                  (see dsmem_hist_partials) */
+                                  2^24 keys, on the SMs its clusters leave idle (see
+                                  dsmem_hist_partials) */
   int64_t partial_stride;      /* u32 elements between two partial rows (num_bins rounded up to 4) */
-  int64_t workspace_bytes;     /* scratch: partial_rows * partial_stride * 4, plus 16 bytes of
-                                  tile counter with the helper */
+  int64_t workspace_bytes;     /* scratch: partial_rows * partial_stride * 4, plus 32 bytes of
+                                  tile counter and timing with the helper */
 } dsmem_hist_plan_t;
 
 /* Planner overrides; a zero field (or -1 for `aggregate` and `kernel`) means "choose". */
@@ -205,18 +205,23 @@ DSMEM_HIST_API int dsmem_hist_host(const int32_t* h_keys, int64_t n, int32_t num
  * Memory", section "The cluster histogram": zero, barrier, DSMEM increments,
  * barrier, flush).  Row c < num_clusters is cluster c's.  With a helper row
  * (partial_rows == num_clusters + 1: a single-pass ship plan of at least
- * 2^24 keys, no hot bin, and SMs left idle by the clusters) a global-atomic
+ * 2^24 keys that leaves SMs idle) a global-atomic
  * helper kernel runs beside the clusters on the idle SMs, on a second
  * stream of the library forked from and joined back into `stream`: the
  * clusters' rounds take the first tiles of the keys, the helper the rest
  * ("When it beats global atomics": one global atomic per key, into the last
  * row), and clusters that finish early take the helper's tiles it has not
- * claimed yet.  DSMEM_HIST_HELPER=0 in the environment makes the planner
- * leave the helper out.
+ * claimed yet.  The helper's share of the tiles starts from the idle SMs'
+ * expected pace and then follows what earlier launches on the same stream
+ * report: the first cluster CTA done with its rounds computes, from the
+ * GPU's global timer, the share at which both sides would have finished
+ * together.  DSMEM_HIST_HELPER=0 in the environment makes the planner leave
+ * the helper out.
  *   plan      from dsmem_hist_plan for the same num_bins (checked for
  *             consistency; EINVAL otherwise)
  *   partials  device, 16-byte aligned, plan->workspace_bytes bytes: the
- *             partial rows, then (helper) a tile counter the call zeroes;
+ *             partial rows, then (helper) a tile counter and timing words
+ *             the call zeroes;
  *             with accumulate == 1 the rows must hold those of an earlier
  *             call with the same plan (used to fold key chunks into one
  *             histogram)

@@ -137,7 +137,7 @@ def test_planner_covers_every_bin(nb, slice_cap):
         helper = p["partial_rows"] - p["num_clusters"]
         assert helper in (0, 1)                            # the helper's row, if any
         assert not helper or (p["kernel"] == pkg.KERNEL_SHIP and passes == 1)
-        assert p["workspace_bytes"] == p["partial_rows"] * p["partial_stride"] * 4 + 16 * helper
+        assert p["workspace_bytes"] == p["partial_rows"] * p["partial_stride"] * 4 + 32 * helper
         assert p["smem_bytes"] <= GB300["max_smem_per_block_optin"]
         if p["kernel"] == pkg.KERNEL_SHIP:
             assert P >= 2 and p["block_threads"] == pkg.SHIP_THREADS
@@ -290,7 +290,7 @@ def test_planner_hot_bin_hint():
     skip = ("hot_bin", "partial_rows", "workspace_bytes")
     assert {k: v for k, v in h.items() if k not in skip} == \
         {k: v for k, v in p.items() if k not in skip}   # same shape otherwise
-    assert h["partial_rows"] == h["num_clusters"]           # a hot bin leaves the helper out
+    assert h["partial_rows"] == p["partial_rows"]           # the helper runs with either kernel
     assert plan(GB300, 262144, 1 << 28, 15, hot_bin=0)["hot_bin"] == 0
     # the direct kernel ignores the hint
     assert plan(GB300, 262144, 1 << 28, 15, hot_bin=7, kernel=pkg.KERNEL_DIRECT)["hot_bin"] == -1
@@ -305,9 +305,9 @@ def test_planner_helper_row():
     plans of at least 2^24 keys without a hot bin that leave SMs idle."""
     rows = lambda p: (p["partial_rows"], p["workspace_bytes"])
     p = plan(GB300, 262144, 1 << 28, 15, cluster_size=8)   # 15 clusters of 8: 32 SMs idle
-    assert p["num_clusters"] == 15 and rows(p) == (16, 16 * 262144 * 4 + 16)
+    assert p["num_clusters"] == 15 and rows(p) == (16, 16 * 262144 * 4 + 32)
     r = plan(GB300, 524288, 1 << 30, 7, cluster_size=16)   # 7 clusters of 16: 40 SMs idle
-    assert rows(r) == (8, 8 * 524288 * 4 + 16)
+    assert rows(r) == (8, 8 * 524288 * 4 + 32)
     small = plan(GB300, 262144, (1 << 24) - 1, 15, cluster_size=8)
     assert small["partial_rows"] == small["num_clusters"]  # too few keys
     assert plan(GB300, 262144, 1 << 24, 15, cluster_size=8)["partial_rows"] == 16
@@ -316,6 +316,6 @@ def test_planner_helper_row():
     multi = plan(GB300, 1 << 22, 1 << 28, 0, cluster_size=16)
     assert multi["passes"] > 1 and multi["partial_rows"] == multi["num_clusters"]
     hot = plan(GB300, 262144, 1 << 28, 15, cluster_size=8, hot_bin=5)
-    assert rows(hot) == (15, 15 * 262144 * 4)
+    assert rows(hot) == rows(p)                            # the hot-bin kernel takes it too
     direct = plan(GB300, 262144, 1 << 28, 15, cluster_size=8, kernel=pkg.KERNEL_DIRECT)
     assert direct["partial_rows"] == direct["num_clusters"]
