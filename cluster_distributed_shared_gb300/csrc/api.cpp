@@ -619,9 +619,10 @@ int check_plan(const DeviceState* st, const dsmem_hist_plan_t* p, int32_t num_bi
       (p->hot_bin >= 0 && p->kernel != DSMEM_HIST_KERNEL_SHIP))
     return fail(DSMEM_HIST_EINVAL, "plan: hot_bin must be -1 or a bin of a ship-kernel plan");
   if (p->partial_rows != p->num_clusters &&
-      !(p->partial_rows == p->num_clusters + 1 && p->kernel == DSMEM_HIST_KERNEL_SHIP && p->passes == 1))
+      !(p->partial_rows == p->num_clusters + 1 && p->kernel == DSMEM_HIST_KERNEL_SHIP && p->passes == 1 &&
+        p->keys_per_thread == 8))
     return fail(DSMEM_HIST_EINVAL, "plan: partial_rows must be num_clusters, or num_clusters + 1 "
-                "(the helper's row) for a single-pass ship plan");
+                "(the helper's row) for a single-pass ship plan with 8 keys per thread");
   return DSMEM_HIST_OK;
 }
 

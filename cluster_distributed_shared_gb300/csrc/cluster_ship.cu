@@ -252,19 +252,22 @@ __device__ __forceinline__ uint4 pad_vector(uint32_t pad0) {
 // together.  rho is how far the helper's pace carried it through its range
 // by now: the ratio of the times since the launch started when the helper
 // kernel has finished already, else the fraction of its tiles claimed.
-// With helper share f the target is rho f / (rho f + 1 - f).
-__device__ __noinline__ void report_helper_share(const ClusterHistArgs& a, uint32_t claimed) {
-  const unsigned long long* times = reinterpret_cast<const unsigned long long*>(a.queue + 2);
+// With helper share f the target is rho f / (rho f + 1 - f).  (Scalars by
+// value: a reference to the kernel's arguments would move them to local
+// memory.)
+__device__ __forceinline__ void report_helper_share(const uint32_t* queue, uint32_t helper_tiles,
+                                                 uint32_t cluster_tiles, unsigned long long* report,
+                                                 uint32_t seq, uint32_t claimed) {
+  const unsigned long long* times = reinterpret_cast<const unsigned long long*>(queue + 2);
   const unsigned long long now = global_timer_ns();
   const unsigned long long t0 = ld_volatile_u64(times), th = ld_volatile_u64(times + 1);
-  if (a.helper_tiles == 0 || a.cluster_tiles == 0 || t0 == 0 || now <= t0) return;
-  const float H = static_cast<float>(a.helper_tiles), C = static_cast<float>(a.cluster_tiles);
+  if (helper_tiles == 0 || cluster_tiles == 0 || t0 == 0 || now <= t0) return;
+  const float H = static_cast<float>(helper_tiles), C = static_cast<float>(cluster_tiles);
   const float rho = th > t0 && th <= now ? static_cast<float>(now - t0) / static_cast<float>(th - t0)
                                          : fminf(static_cast<float>(claimed), H) / H;
   const float f = H / (H + C);
   const float target = rho * f / (rho * f + 1.0f - f);
-  st_volatile_u64(a.helper_report,
-                  (static_cast<unsigned long long>(a.helper_seq) << 32) | __float_as_uint(target));
+  st_volatile_u64(report, (static_cast<unsigned long long>(seq) << 32) | __float_as_uint(target));
 }
 
 // Loads a warp's consecutive tiles t0, t0 + 1, ... of a round; tiles past
@@ -285,7 +288,10 @@ __device__ __forceinline__ void load_round(int4 (&v)[kKpt / 4], const int4* vec,
   }
 }
 
-template <int kKpt, bool kPow2, bool kSkew>
+// kHelper: the instantiation launched beside the idle-SM helper (single-pass
+// launches with 8 keys per thread); only it carries the mop-up, so the
+// others compile to the same code as without a helper.
+template <int kKpt, bool kPow2, bool kSkew, bool kHelper>
 __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const ClusterHistArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   Ctx c;
@@ -336,7 +342,7 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
   const uint32_t nwarps = gridDim.x * kWarps;
   const uint32_t gwarp = blockIdx.x * kWarps + warp;
   const uint32_t ntiles = static_cast<uint32_t>(((a.n - a.head) >> 2) >> 5);
-  const uint32_t ctiles = min(ntiles, a.cluster_tiles);
+  const uint32_t ctiles = kHelper ? min(ntiles, a.cluster_tiles) : ntiles;
   const int4* vec = reinterpret_cast<const int4*>(a.keys + a.head) + c.lane;
   constexpr int kTiles = kKpt / 4;
   const uint32_t per_round = nwarps * kTiles;
@@ -389,8 +395,10 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
     }
     if (threadIdx.x < 32u) st_shared_u32(header0 + 4u * threadIdx.x, 0u);
     if (threadIdx.x == 0) st_shared_u32(gave_up, 0u);
-    if (a.queue != nullptr && pass == 0 && rank == 0 && threadIdx.x == 0)
-      atomicCAS(reinterpret_cast<unsigned long long*>(a.queue + 2), 0ull, global_timer_ns());
+    if constexpr (kHelper) {
+      if (pass == 0 && rank == 0 && threadIdx.x == 0)
+        atomicCAS(reinterpret_cast<unsigned long long*>(a.queue + 2), 0ull, global_timer_ns());
+    }
     if (threadIdx.x == 0) {
       // One arrival per other sender and round; their bytes complete it.
       mbar_init(full0, P - 1u);
@@ -485,7 +493,7 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
       }
     }
 
-    if (a.queue != nullptr) {
+    if constexpr (kHelper) {
       // Mop-up (single-pass launches with a helper): the helper's tiles
       // [cluster_tiles, ntiles) are claimed kMopTiles at a time from the
       // counter the helper claims from, and each key goes straight to its
@@ -503,7 +511,8 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
         st_shared_u32(slot0, first);
         // The first CTA done with its rounds reports how the split went.
         if (a.helper_report != nullptr && atomicCAS(a.queue + 1, 0u, 1u) == 0u)
-          report_helper_share(a, first);
+          report_helper_share(a.queue, a.helper_tiles, a.cluster_tiles, a.helper_report,
+                              a.helper_seq, first);
       }
       __syncthreads();
       uint32_t t0 = ld_shared_u32(slot0);
@@ -678,12 +687,17 @@ __global__ void __launch_bounds__(kHelperThreads, 1) ship_helper_kernel(const Cl
     atomicExch(reinterpret_cast<unsigned long long*>(a.queue + 4), global_timer_ns());
 }
 
-template <int kKpt, bool kPow2, bool kSkew>
+template <int kKpt, bool kPow2, bool kSkew, bool kHelper = false>
 void* kernel_ptr_t() {
-  return reinterpret_cast<void*>(&cluster_ship_kernel<kKpt, kPow2, kSkew>);
+  return reinterpret_cast<void*>(&cluster_ship_kernel<kKpt, kPow2, kSkew, kHelper>);
 }
 
-void* ship_kernel_ptr(int kpt, bool pow2, bool skew) {
+// The helper instantiations exist for 8 keys per thread only.
+void* ship_kernel_ptr(int kpt, bool pow2, bool skew, bool helper = false) {
+  if (helper) {
+    if (skew) return pow2 ? kernel_ptr_t<8, true, true, true>() : kernel_ptr_t<8, false, true, true>();
+    return pow2 ? kernel_ptr_t<8, true, false, true>() : kernel_ptr_t<8, false, false, true>();
+  }
   if (skew) {
     if (kpt == 8) return pow2 ? kernel_ptr_t<8, true, true>() : kernel_ptr_t<8, false, true>();
     return pow2 ? kernel_ptr_t<4, true, true>() : kernel_ptr_t<4, false, true>();
@@ -704,8 +718,8 @@ cudaError_t read_and_clear_ship_status(uint32_t* out) {
 }
 
 cudaError_t prepare_ship_kernel(int kpt, int smem_bytes) {
-  for (int v = 0; v < 4; ++v) {
-    const void* fn = ship_kernel_ptr(kpt, (v & 1) != 0, (v & 2) != 0);
+  for (int v = 0; v < (kpt == 8 ? 8 : 4); ++v) {
+    const void* fn = ship_kernel_ptr(kpt, (v & 1) != 0, (v & 2) != 0, (v & 4) != 0);
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -754,18 +768,26 @@ cudaError_t launch_cluster_ship(const dsmem_hist_plan_t& plan, const ClusterHist
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const bool p2 = is_pow2(plan.bins_per_cta);
+  if (args.queue != nullptr) {  // beside the helper (8 keys per thread; the planner sees to it)
+    if (plan.keys_per_thread != 8) return cudaErrorInvalidValue;
+    if (args.hot_bin != kNoHot)
+      return p2 ? cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, true, true, true>, args)
+                : cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, false, true, true>, args);
+    return p2 ? cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, true, false, true>, args)
+              : cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, false, false, true>, args);
+  }
   if (args.hot_bin != kNoHot) {
     if (plan.keys_per_thread == 8)
-      return p2 ? cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, true, true>, args)
-                : cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, false, true>, args);
-    return p2 ? cudaLaunchKernelEx(&cfg, cluster_ship_kernel<4, true, true>, args)
-              : cudaLaunchKernelEx(&cfg, cluster_ship_kernel<4, false, true>, args);
+      return p2 ? cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, true, true, false>, args)
+                : cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, false, true, false>, args);
+    return p2 ? cudaLaunchKernelEx(&cfg, cluster_ship_kernel<4, true, true, false>, args)
+              : cudaLaunchKernelEx(&cfg, cluster_ship_kernel<4, false, true, false>, args);
   }
   if (plan.keys_per_thread == 8)
-    return p2 ? cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, true, false>, args)
-              : cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, false, false>, args);
-  return p2 ? cudaLaunchKernelEx(&cfg, cluster_ship_kernel<4, true, false>, args)
-            : cudaLaunchKernelEx(&cfg, cluster_ship_kernel<4, false, false>, args);
+    return p2 ? cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, true, false, false>, args)
+              : cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, false, false, false>, args);
+  return p2 ? cudaLaunchKernelEx(&cfg, cluster_ship_kernel<4, true, false, false>, args)
+            : cudaLaunchKernelEx(&cfg, cluster_ship_kernel<4, false, false, false>, args);
 }
 
 cudaError_t prepare_ship_helper() {

@@ -20,6 +20,10 @@ N, BINS, STEPS = 1_048_576, 8_192, 20
 
 @pytest.fixture(scope="module")
 def line():
+    if ROOT not in sys.path:
+        sys.path.insert(0, ROOT)
+    import __graft_entry__
+    __graft_entry__.build()   # the child process imports what this builds
     cmd = [sys.executable, "bench.py", "--workload", "uniform-1M-8K", "--steps", str(STEPS),
            "--warmup", "3", "--cpu-seconds", "0.5", "--e2e-steps", "3"]
     out = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=900)

@@ -568,3 +568,55 @@ def test_idle_sm_helper_and_mop_up(monkeypatch, mode, share):
         assert np.array_equal(pkg.dsmem_hist_host(keys, num_bins), want)
         del d, sub
     assert pkg.dsmem_hist_device_status() == 0
+
+
+_SHARE_SCRIPT = r"""
+import sys, numpy as np, torch
+sys.path.insert(0, sys.argv[1])
+import cluster_distributed_shared_gb300 as pkg, gen, oracle
+n, nb = 1 << 26, 262144
+for name, keys in [("zipf", gen.zipf(n, nb, seed=91)), ("uniform", gen.uniform(n, nb, seed=92))]:
+    want = oracle.histogram(keys, nb)
+    d = torch.from_numpy(keys).cuda()
+    s = torch.cuda.Stream()
+    print("WORKLOAD", name, file=sys.stderr, flush=True)
+    for i in range(8):
+        got = pkg.dsmem_hist(d, nb, stream=s, cluster_size=8)
+        s.synchronize()                      # the next call reads this one's report
+        ok = np.array_equal(got.cpu().numpy().view(np.uint32), want)
+        print("PARITY", name, i, ok, file=sys.stderr, flush=True)
+"""
+
+
+def test_helper_share_follows_the_reports():
+    """The helper's share starts from the idle SMs' expected pace and then
+    follows each launch's report on the same stream: on Zipf keys (its cache
+    counts the frequent keys in shared memory) it grows well past the prior,
+    on uniform keys (a fresh stream) it settles near the prior; every call is
+    exact."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, DSMEM_HIST_TRACE="1")
+    out = subprocess.run([sys.executable, "-c", _SHARE_SCRIPT, root], env=env, capture_output=True,
+                         text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-3000:]
+    shares, current = {}, None
+    for l in out.stderr.splitlines():
+        if l.startswith("WORKLOAD"):
+            current = l.split()[1]
+            shares[current] = []
+        elif l.startswith("PARITY"):
+            assert l.split()[3] == "True", l
+        elif "reports share" in l and current is not None:
+            # "... reports share T -> share BEFORE -> AFTER"
+            parts = l.split("->")
+            shares[current].append((float(parts[1].split()[1]), float(parts[2])))
+    for name in ("zipf", "uniform"):
+        assert len(shares[name]) >= 6, shares            # one report per call after the first
+        prior = shares[name][0][0]
+        assert 0.05 < prior < 0.2                         # idle SMs x pace / all SMs
+        assert all(0.01 <= after <= 0.6 for _, after in shares[name])
+    assert shares["zipf"][-1][1] > 1.5 * shares["zipf"][0][0]
+    assert 0.5 * shares["uniform"][0][0] < shares["uniform"][-1][1] < 2.0 * shares["uniform"][0][0]
