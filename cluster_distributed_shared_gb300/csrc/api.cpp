@@ -56,11 +56,17 @@ struct DeviceState {
   // (kernel, variant, threads, smem) -> largest co-schedulable cluster size
   std::map<std::tuple<int, int, int, int>, int> potential;
   std::mutex host_call;  // serialises dsmem_hist_host on this device
-  // The helper kernel's stream (lowest priority, so the clusters launched
-  // first keep their SMs) and its fork and join events; helper_call
-  // serialises their use.
-  cudaStream_t helper_stream = nullptr;
-  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  // The helper kernel's streams (lowest priority, so the clusters launched
+  // first keep their SMs) and their fork and join events, one set per
+  // caller-stream slot, so that calls on different streams do not queue
+  // behind each other's helpers; helper_call serialises their use.  Calls
+  // without a stream slot use the last set.
+  struct HelperStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+  };
+  HelperStream helper_streams[kStatusSlots + 1] = {};
+  bool helper_prepared = false;
   std::mutex helper_call;
   // Per stream slot, under helper_call: the helper's current share of the
   // tiles (0: none learned yet), the last report taken, and the last
@@ -360,13 +366,17 @@ cudaError_t launch_plan(const dsmem_hist_plan_t& plan, ClusterHistArgs args, cud
 
   cudaError_t e;
   std::lock_guard<std::mutex> g(st->helper_call);
-  if (!st->helper_stream) {
+  if (!st->helper_prepared) {
+    if ((e = prepare_ship_helper()) != cudaSuccess) return e;
+    st->helper_prepared = true;
+  }
+  DeviceState::HelperStream& hs = st->helper_streams[sr && sr->slot >= 0 ? sr->slot : kStatusSlots];
+  if (!hs.stream) {
     int least = 0, greatest = 0;
-    if ((e = prepare_ship_helper()) != cudaSuccess ||
-        (e = cudaDeviceGetStreamPriorityRange(&least, &greatest)) != cudaSuccess ||
-        (e = cudaStreamCreateWithPriority(&st->helper_stream, cudaStreamNonBlocking, least)) != cudaSuccess ||
-        (e = cudaEventCreateWithFlags(&st->ev_fork, cudaEventDisableTiming)) != cudaSuccess ||
-        (e = cudaEventCreateWithFlags(&st->ev_join, cudaEventDisableTiming)) != cudaSuccess)
+    if ((e = cudaDeviceGetStreamPriorityRange(&least, &greatest)) != cudaSuccess ||
+        (e = cudaStreamCreateWithPriority(&hs.stream, cudaStreamNonBlocking, least)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&hs.fork, cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&hs.join, cudaEventDisableTiming)) != cudaSuccess)
       return e;
   }
   const int active = plan.num_clusters * plan.cluster_size;
@@ -393,15 +403,15 @@ cudaError_t launch_plan(const dsmem_hist_plan_t& plan, ClusterHistArgs args, cud
   // helper's CTAs fill the idle ones; a cluster that still finds no room
   // starts later, and the mop-up balances the work either way.
   if ((e = cudaMemsetAsync(args.queue, 0, kHelperQueueBytes, stream)) != cudaSuccess ||
-      (e = cudaEventRecord(st->ev_fork, stream)) != cudaSuccess ||
-      (e = cudaStreamWaitEvent(st->helper_stream, st->ev_fork, 0)) != cudaSuccess ||
+      (e = cudaEventRecord(hs.fork, stream)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(hs.stream, hs.fork, 0)) != cudaSuccess ||
       (!args.accumulate &&
-       (e = cudaMemsetAsync(row, 0, sizeof(uint32_t) * args.stride, st->helper_stream)) != cudaSuccess) ||
+       (e = cudaMemsetAsync(row, 0, sizeof(uint32_t) * args.stride, hs.stream)) != cudaSuccess) ||
       (e = launch_cluster_ship(plan, args, stream)) != cudaSuccess ||
-      (e = launch_ship_helper(args, row, idle, st->helper_stream)) != cudaSuccess ||
-      (e = cudaEventRecord(st->ev_join, st->helper_stream)) != cudaSuccess)
+      (e = launch_ship_helper(args, row, idle, hs.stream)) != cudaSuccess ||
+      (e = cudaEventRecord(hs.join, hs.stream)) != cudaSuccess)
     return e;
-  return cudaStreamWaitEvent(stream, st->ev_join, 0);
+  return cudaStreamWaitEvent(stream, hs.join, 0);
 }
 
 // Plans for the current device, confirming the shape with the occupancy
@@ -1065,13 +1075,13 @@ void dsmem_hist_release(void) {
       for (int i = 0; i < kStatusSlots; ++i)
         st->slot_seq[i] = st->slot_bins_since[i] = 0, st->slot_bins[i] = 0;
     }
-    if (st->helper_stream) {
-      cudaStreamSynchronize(st->helper_stream);
-      cudaStreamDestroy(st->helper_stream);
-      cudaEventDestroy(st->ev_fork);
-      cudaEventDestroy(st->ev_join);
-      st->helper_stream = nullptr;
-      st->ev_fork = st->ev_join = nullptr;
+    for (auto& hs : st->helper_streams) {
+      if (!hs.stream) continue;
+      cudaStreamSynchronize(hs.stream);
+      cudaStreamDestroy(hs.stream);
+      cudaEventDestroy(hs.fork);
+      cudaEventDestroy(hs.join);
+      hs = DeviceState::HelperStream{};
     }
     if (st->copy_stream) {
       cudaStreamDestroy(st->copy_stream);
