@@ -69,9 +69,10 @@ struct DeviceState {
   bool helper_prepared = false;
   std::mutex helper_call;
   // Per stream slot, under helper_call: the helper's current share of the
-  // tiles (0: none learned yet), the last report taken, and the last
-  // sequence number handed out.
-  double helper_share[kStatusSlots] = {};
+  // tiles beside the default and beside the hot-bin kernel (0: none learned
+  // yet; the best shares differ), the last report taken, and the last
+  // sequence number handed out (2 * launch count + kind).
+  double helper_share[kStatusSlots][2] = {};
   uint32_t helper_taken[kStatusSlots] = {};
   uint32_t helper_seq[kStatusSlots] = {};
   // Per-stream words in pinned, host-mapped memory (h_status on the host,
@@ -322,16 +323,19 @@ constexpr double kHelperShareMin = 0.01, kHelperShareMax = 0.6;
 // first CTA done with its rounds, the share at which the helper and the
 // clusters would have finished together (report_helper_share in the ship
 // kernel); a new report moves the share three quarters of the way to it.
+// Shares are kept apart for the default (kind 0) and the hot-bin kernel
+// (kind 1); a report's sequence number carries its kind in bit 0.
 // st->helper_call must be held.
-double helper_share(DeviceState* st, const SlotRef* sr, double prior) {
+double helper_share(DeviceState* st, const SlotRef* sr, int kind, double prior) {
   if (!sr || sr->slot < 0 || !sr->h_helper) return prior;
   const int slot = sr->slot;
-  double& share = st->helper_share[slot];
-  if (share <= 0.0) share = prior;
+  for (double& s : st->helper_share[slot])
+    if (s <= 0.0) s = prior;
   const unsigned long long w = *reinterpret_cast<volatile unsigned long long*>(sr->h_helper);
   const uint32_t seq = static_cast<uint32_t>(w >> 32), bits = static_cast<uint32_t>(w);
   if (seq != 0 && seq != st->helper_taken[slot]) {
     st->helper_taken[slot] = seq;
+    double& share = st->helper_share[slot][seq & 1u];
     float target = 0.0f;
     memcpy(&target, &bits, sizeof target);
     if (target > 0.0f && target < 1.0f) {
@@ -339,11 +343,11 @@ double helper_share(DeviceState* st, const SlotRef* sr, double prior) {
       share = 0.25 * share + 0.75 * target;
       share = share < kHelperShareMin ? kHelperShareMin : (share > kHelperShareMax ? kHelperShareMax : share);
       if (trace_enabled())
-        fprintf(stderr, "[dsmem_hist] stream slot %d: helper launch %u reports share %.4f -> share "
-                "%.4f -> %.4f\n", slot, seq, target, before, share);
+        fprintf(stderr, "[dsmem_hist] stream slot %d: helper launch %u (kind %u) reports share %.4f "
+                "-> share %.4f -> %.4f\n", slot, seq >> 1, seq & 1u, target, before, share);
     }
   }
-  return share;
+  return st->helper_share[slot][kind];
 }
 
 // Launches a plan.  With `st` non-null and a helper row in the plan
@@ -381,7 +385,8 @@ cudaError_t launch_plan(const dsmem_hist_plan_t& plan, ClusterHistArgs args, cud
   }
   const int active = plan.num_clusters * plan.cluster_size;
   const int idle = st->dev.sm_count > active ? st->dev.sm_count - active : 0;
-  double share = helper_share(st, sr, idle * kHelperRelativeRate / (active + idle * kHelperRelativeRate));
+  const int kind = args.hot_bin != 0xFFFFFFFFu ? 1 : 0;
+  double share = helper_share(st, sr, kind, idle * kHelperRelativeRate / (active + idle * kHelperRelativeRate));
   if (const char* v = getenv("DSMEM_HIST_HELPER_SHARE")) share = atof(v);  // sweeps
   share = share < 0.0 ? 0.0 : (share > 1.0 ? 1.0 : share);
   const uint64_t per_round = static_cast<uint64_t>(active) * (kShipThreads / 32) * (plan.keys_per_thread / 4);
@@ -391,13 +396,14 @@ cudaError_t launch_plan(const dsmem_hist_plan_t& plan, ClusterHistArgs args, cud
   uint32_t* row = args.partials + static_cast<size_t>(plan.num_clusters) * args.stride;
   args.queue = args.partials + static_cast<size_t>(plan.partial_rows) * args.stride;
   if (sr && sr->slot >= 0 && sr->d_helper) {
-    // A new sequence number tells this launch's report from older ones.
+    // A new sequence number tells this launch's report from older ones;
+    // bit 0 is the kernel kind.
     const int slot = sr->slot;
-    uint32_t seq = st->helper_seq[slot] + 1;
-    if (seq == 0) seq = 1;
+    uint32_t seq = st->helper_seq[slot] + 2u;
+    if (seq < 2u) seq = 2u;
     st->helper_seq[slot] = seq;
     args.helper_report = sr->d_helper;
-    args.helper_seq = seq;
+    args.helper_seq = seq | static_cast<uint32_t>(kind);
   }
   // The clusters are launched first, so they take their SMs before the
   // helper's CTAs fill the idle ones; a cluster that still finds no room
