@@ -62,8 +62,9 @@ struct DeviceState {
   // behind each other's helpers; helper_call serialises their use.  Calls
   // without a stream slot use the last set.
   struct HelperStream {
-    cudaStream_t stream = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
+    cudaStream_t stream = nullptr;         // the helper's, lowest priority
+    cudaStream_t cluster_stream = nullptr; // the cluster kernel's, highest priority
+    cudaEvent_t fork = nullptr, clusters_done = nullptr, join = nullptr;
   };
   HelperStream helper_streams[kStatusSlots + 1] = {};
   bool helper_prepared = false;
@@ -73,6 +74,13 @@ struct DeviceState {
   // yet; the best shares differ), the last report taken, and the last
   // sequence number handed out (2 * launch count + kind).
   double helper_share[kStatusSlots][2] = {};
+  // The step towards a report (0: not started), and the sign of the last
+  // correction, per slot and kind.
+  double helper_gain[kStatusSlots][2] = {};
+  int helper_last_sign[kStatusSlots][2] = {};
+  // The first launch (count) that ran with the current share, per slot and
+  // kind: reports of earlier launches describe an older share.
+  uint32_t helper_valid_from[kStatusSlots][2] = {};
   uint32_t helper_taken[kStatusSlots] = {};
   uint32_t helper_seq[kStatusSlots] = {};
   // Per-stream words in pinned, host-mapped memory (h_status on the host,
@@ -317,15 +325,25 @@ int prepare_locked(DeviceState* st, const dsmem_hist_plan_t& p) {
 // share of the tiles until a stream has reported how the split went.
 constexpr double kHelperRelativeRate = 0.42;
 constexpr double kHelperShareMin = 0.01, kHelperShareMax = 0.6;
+constexpr double kHelperGainMin = 0.05, kHelperGainMax = 0.75;
 
 // The helper's share for the next launch on the stream of `sr`: the share it
 // has learned, else `prior`.  Each launch with a helper reports, from the
 // first CTA done with its rounds, the share at which the helper and the
 // clusters would have finished together (report_helper_share in the ship
-// kernel); a new report moves the share three quarters of the way to it.
-// Shares are kept apart for the default (kind 0) and the hot-bin kernel
-// (kind 1); a report's sequence number carries its kind in bit 0.
-// st->helper_call must be held.
+// kernel); a new report moves the share part of the way to it.  The step
+// starts at three quarters, halves (down to kHelperGainMin) whenever the
+// correction changes direction and grows again by a quarter while it keeps
+// its direction: where the helper's pace depends on which tiles it gets
+// (runs in the last half of the keys and uniform keys before them: the
+// reported target then moves several times as far as the share), full steps
+// made the share swing around its optimum by a quarter.  Shares are kept
+// apart for the default (kind 0) and the hot-bin kernel (kind 1); a report's
+// sequence number carries its kind in bit 0 and the launch count above it.
+// A report counts only if its launch ran with the current share: calls
+// enqueued far ahead of the GPU see reports of launches made with an older
+// share, and acting on those made the share overshoot.  st->helper_call
+// must be held.
 double helper_share(DeviceState* st, const SlotRef* sr, int kind, double prior) {
   if (!sr || sr->slot < 0 || !sr->h_helper) return prior;
   const int slot = sr->slot;
@@ -333,15 +351,28 @@ double helper_share(DeviceState* st, const SlotRef* sr, int kind, double prior) 
     if (s <= 0.0) s = prior;
   const unsigned long long w = *reinterpret_cast<volatile unsigned long long*>(sr->h_helper);
   const uint32_t seq = static_cast<uint32_t>(w >> 32), bits = static_cast<uint32_t>(w);
-  if (seq != 0 && seq != st->helper_taken[slot]) {
+  const uint32_t k = seq & 1u;
+  if (seq != 0 && seq != st->helper_taken[slot] &&
+      static_cast<int32_t>((seq >> 1) - st->helper_valid_from[slot][k]) >= 0) {
     st->helper_taken[slot] = seq;
-    double& share = st->helper_share[slot][seq & 1u];
+    double& share = st->helper_share[slot][k];
+    double& gain = st->helper_gain[slot][k];
+    int& last_sign = st->helper_last_sign[slot][k];
     float target = 0.0f;
     memcpy(&target, &bits, sizeof target);
     if (target > 0.0f && target < 1.0f) {
       const double before = share;
-      share = 0.25 * share + 0.75 * target;
+      const int sign = target > share ? 1 : -1;
+      if (gain <= 0.0)
+        gain = kHelperGainMax;
+      else if (last_sign != 0 && sign != last_sign)
+        gain = gain * 0.5 < kHelperGainMin ? kHelperGainMin : gain * 0.5;
+      else
+        gain = gain * 1.25 > kHelperGainMax ? kHelperGainMax : gain * 1.25;
+      last_sign = sign;
+      share += gain * (target - share);
       share = share < kHelperShareMin ? kHelperShareMin : (share > kHelperShareMax ? kHelperShareMax : share);
+      if (share != before) st->helper_valid_from[slot][k] = (st->helper_seq[slot] >> 1) + 1u;
       if (trace_enabled())
         fprintf(stderr, "[dsmem_hist] stream slot %d: helper launch %u (kind %u) reports share %.4f "
                 "-> share %.4f -> %.4f\n", slot, seq >> 1, seq & 1u, target, before, share);
@@ -351,14 +382,15 @@ double helper_share(DeviceState* st, const SlotRef* sr, int kind, double prior) 
 }
 
 // Launches a plan.  With `st` non-null and a helper row in the plan
-// (partial_rows > num_clusters), the ship kernel's rounds cover the first
+// (partial_rows > num_clusters), the ship kernel is launched on the first
 // tiles and the global-atomic helper, on the SMs the clusters leave idle,
 // takes the rest: its share starts at what the idle SMs would finish in the
 // time the clusters take for theirs and then follows the stream's reports
-// (helper_share); the clusters' rounds are rounded down to whole rounds.
+// (helper_share); the clusters' tiles are rounded down to whole rounds.
 // The helper runs on a second stream forked from and joined back into
 // `stream`; the tile counter is zeroed on `stream` before the fork and the
-// helper's row on the helper stream (unless accumulating).
+// helper's row on the helper stream (unless accumulating).  The mop-up
+// kernel follows the cluster kernel on `stream`.
 cudaError_t launch_plan(const dsmem_hist_plan_t& plan, ClusterHistArgs args, cudaStream_t stream,
                         DeviceState* st = nullptr, const SlotRef* sr = nullptr) {
   if (plan.kernel != DSMEM_HIST_KERNEL_SHIP) return launch_cluster_hist(plan, args, stream);
@@ -379,7 +411,9 @@ cudaError_t launch_plan(const dsmem_hist_plan_t& plan, ClusterHistArgs args, cud
     int least = 0, greatest = 0;
     if ((e = cudaDeviceGetStreamPriorityRange(&least, &greatest)) != cudaSuccess ||
         (e = cudaStreamCreateWithPriority(&hs.stream, cudaStreamNonBlocking, least)) != cudaSuccess ||
+        (e = cudaStreamCreateWithPriority(&hs.cluster_stream, cudaStreamNonBlocking, greatest)) != cudaSuccess ||
         (e = cudaEventCreateWithFlags(&hs.fork, cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&hs.clusters_done, cudaEventDisableTiming)) != cudaSuccess ||
         (e = cudaEventCreateWithFlags(&hs.join, cudaEventDisableTiming)) != cudaSuccess)
       return e;
   }
@@ -405,17 +439,30 @@ cudaError_t launch_plan(const dsmem_hist_plan_t& plan, ClusterHistArgs args, cud
     args.helper_report = sr->d_helper;
     args.helper_seq = seq | static_cast<uint32_t>(kind);
   }
-  // The clusters are launched first, so they take their SMs before the
-  // helper's CTAs fill the idle ones; a cluster that still finds no room
-  // starts later, and the mop-up balances the work either way.
+  // The counter and the helper's row are zeroed on `stream` before the
+  // fork.  Then the cluster kernel goes on the highest-priority stream and
+  // the helper on the lowest, both forked from `stream`: when both are ready
+  // to start, the clusters' CTAs are dispatched first, and the helper's CTAs
+  // fill the SMs they leave idle.  (When the helper's CTAs, or a memset's,
+  // got to SMs a cluster needed first, that cluster waited for the helper,
+  // and some streams settled at 1.72 instead of 1.31 ms on the run-heavy
+  // workload.)  The mop-up kernel follows the cluster kernel on `stream` and
+  // takes the helper's tiles it has not claimed by then.  The cluster kernel
+  // sees only its own tiles (and the unaligned head).
+  ClusterHistArgs cargs = args;
+  cargs.n = static_cast<int64_t>(args.head) + (static_cast<int64_t>(args.cluster_tiles) << 7);
   if ((e = cudaMemsetAsync(args.queue, 0, kHelperQueueBytes, stream)) != cudaSuccess ||
-      (e = cudaEventRecord(hs.fork, stream)) != cudaSuccess ||
-      (e = cudaStreamWaitEvent(hs.stream, hs.fork, 0)) != cudaSuccess ||
       (!args.accumulate &&
-       (e = cudaMemsetAsync(row, 0, sizeof(uint32_t) * args.stride, hs.stream)) != cudaSuccess) ||
-      (e = launch_cluster_ship(plan, args, stream)) != cudaSuccess ||
+       (e = cudaMemsetAsync(row, 0, sizeof(uint32_t) * args.stride, stream)) != cudaSuccess) ||
+      (e = cudaEventRecord(hs.fork, stream)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(hs.cluster_stream, hs.fork, 0)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(hs.stream, hs.fork, 0)) != cudaSuccess ||
+      (e = launch_cluster_ship(plan, cargs, hs.cluster_stream)) != cudaSuccess ||
+      (e = cudaEventRecord(hs.clusters_done, hs.cluster_stream)) != cudaSuccess ||
       (e = launch_ship_helper(args, row, idle, hs.stream)) != cudaSuccess ||
-      (e = cudaEventRecord(hs.join, hs.stream)) != cudaSuccess)
+      (e = cudaEventRecord(hs.join, hs.stream)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(stream, hs.clusters_done, 0)) != cudaSuccess ||
+      (e = launch_ship_mop_up(args, row, st->dev.sm_count, stream)) != cudaSuccess)
     return e;
   return cudaStreamWaitEvent(stream, hs.join, 0);
 }
@@ -635,10 +682,9 @@ int check_plan(const DeviceState* st, const dsmem_hist_plan_t* p, int32_t num_bi
       (p->hot_bin >= 0 && p->kernel != DSMEM_HIST_KERNEL_SHIP))
     return fail(DSMEM_HIST_EINVAL, "plan: hot_bin must be -1 or a bin of a ship-kernel plan");
   if (p->partial_rows != p->num_clusters &&
-      !(p->partial_rows == p->num_clusters + 1 && p->kernel == DSMEM_HIST_KERNEL_SHIP && p->passes == 1 &&
-        p->keys_per_thread == 8))
+      !(p->partial_rows == p->num_clusters + 1 && p->kernel == DSMEM_HIST_KERNEL_SHIP && p->passes == 1))
     return fail(DSMEM_HIST_EINVAL, "plan: partial_rows must be num_clusters, or num_clusters + 1 "
-                "(the helper's row) for a single-pass ship plan with 8 keys per thread");
+                "(the helper's row) for a single-pass ship plan");
   return DSMEM_HIST_OK;
 }
 
@@ -1084,8 +1130,11 @@ void dsmem_hist_release(void) {
     for (auto& hs : st->helper_streams) {
       if (!hs.stream) continue;
       cudaStreamSynchronize(hs.stream);
+      cudaStreamSynchronize(hs.cluster_stream);
       cudaStreamDestroy(hs.stream);
+      cudaStreamDestroy(hs.cluster_stream);
       cudaEventDestroy(hs.fork);
+      cudaEventDestroy(hs.clusters_done);
       cudaEventDestroy(hs.join);
       hs = DeviceState::HelperStream{};
     }

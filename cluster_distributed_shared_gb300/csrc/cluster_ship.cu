@@ -247,12 +247,13 @@ __device__ __forceinline__ uint4 pad_vector(uint32_t pad0) {
   return make_uint4(pad0, pad0 + 0x00020002u, pad0 + 0x00040004u, pad0 + 0x00060006u);
 }
 
-// Reports, from the first CTA whose rounds are done, the helper's share of
-// the tiles at which the helper and the clusters would have finished
-// together.  rho is how far the helper's pace carried it through its range
-// by now: the ratio of the times since the launch started when the helper
-// kernel has finished already, else the fraction of its tiles claimed.
-// With helper share f the target is rho f / (rho f + 1 - f).  (Scalars by
+// Reports, from the mop-up kernel's first CTA (which starts when the cluster
+// kernel has finished), the helper's share of the tiles at which the helper
+// and the clusters would have finished together.  rho is how far the
+// helper's pace carried it through its range by now: the ratio of the times
+// since the helper started when it has finished already, else the fraction
+// of its tiles claimed.  With helper share f the target is
+// rho f / (rho f + 1 - f).  (Scalars by
 // value: a reference to the kernel's arguments would move them to local
 // memory.)
 __device__ __forceinline__ void report_helper_share(const uint32_t* queue, uint32_t helper_tiles,
@@ -288,10 +289,7 @@ __device__ __forceinline__ void load_round(int4 (&v)[kKpt / 4], const int4* vec,
   }
 }
 
-// kHelper: the instantiation launched beside the idle-SM helper (single-pass
-// launches with 8 keys per thread); only it carries the mop-up, so the
-// others compile to the same code as without a helper.
-template <int kKpt, bool kPow2, bool kSkew, bool kHelper>
+template <int kKpt, bool kPow2, bool kSkew>
 __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const ClusterHistArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   Ctx c;
@@ -334,20 +332,15 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
   // Key stream: warp tiles of 32 vectors (tile t = vectors 32t .. 32t+31),
   // kKpt/4 consecutive tiles per warp per round; tile indices fit 32 bits with room for
   // three rounds on top (the library keeps n below 2^38 for this kernel).
-  // The rounds cover tiles [0, a.cluster_tiles); with a helper (a.queue
-  // non-null) the tiles after them belong to the helper kernel, and this
-  // kernel's CTAs take those the helper has not claimed when their rounds
-  // are done (see the mop-up below).
   constexpr uint32_t kWarps = kShipThreads / 32;
   const uint32_t nwarps = gridDim.x * kWarps;
   const uint32_t gwarp = blockIdx.x * kWarps + warp;
   const uint32_t ntiles = static_cast<uint32_t>(((a.n - a.head) >> 2) >> 5);
-  const uint32_t ctiles = kHelper ? min(ntiles, a.cluster_tiles) : ntiles;
   const int4* vec = reinterpret_cast<const int4*>(a.keys + a.head) + c.lane;
   constexpr int kTiles = kKpt / 4;
   const uint32_t per_round = nwarps * kTiles;
   const uint32_t wtile0 = gwarp * kTiles;  // this warp's first tile of round 0
-  const uint32_t rounds = static_cast<uint32_t>((static_cast<uint64_t>(ctiles) + per_round - 1) / per_round);
+  const uint32_t rounds = static_cast<uint32_t>((static_cast<uint64_t>(ntiles) + per_round - 1) / per_round);
 
   // Ship and apply: warp w serves owner (and sender) w mod P, as member sg of
   // the sng warps that do; lane l of member sg starts at vector 32*sg + l of
@@ -395,10 +388,6 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
     }
     if (threadIdx.x < 32u) st_shared_u32(header0 + 4u * threadIdx.x, 0u);
     if (threadIdx.x == 0) st_shared_u32(gave_up, 0u);
-    if constexpr (kHelper) {
-      if (pass == 0 && rank == 0 && threadIdx.x == 0)
-        atomicCAS(reinterpret_cast<unsigned long long*>(a.queue + 2), 0ull, global_timer_ns());
-    }
     if (threadIdx.x == 0) {
       // One arrival per other sender and round; their bytes complete it.
       mbar_init(full0, P - 1u);
@@ -410,11 +399,11 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
 
     int4 cur[kTiles];
     if (rounds > 0) {
-      load_round<kKpt>(cur, vec, ctiles, wtile0, rounds == 1);
+      load_round<kKpt>(cur, vec, ntiles, wtile0, rounds == 1);
       c.cur_lane = cur_lane0;
       c.lim0 = stage0 + c.blk;
       partition_round<kTiles, kPow2, kSkew>(cur, c, hot_keys);
-      if (rounds > 1) load_round<kKpt>(cur, vec, ctiles, wtile0 + per_round, rounds == 2);
+      if (rounds > 1) load_round<kKpt>(cur, vec, ntiles, wtile0 + per_round, rounds == 2);
     }
     __syncthreads();  // round 0 staged
     uint32_t k = 0;  // r % 3
@@ -477,7 +466,7 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
         c.lim0 = stage0 + (b ^ 1u) * buf_bytes + c.blk;
         partition_round<kTiles, kPow2, kSkew>(cur, c, hot_keys);
         if (r + 2 < rounds)
-          load_round<kKpt>(cur, vec, ctiles, wtile0 + (r + 2) * per_round, r + 3 == rounds);
+          load_round<kKpt>(cur, vec, ntiles, wtile0 + (r + 2) * per_round, r + 3 == rounds);
         __syncwarp();  // the warp's staging stores and cursor updates precede the arrival
         if (c.lane == 0) mbar_arrive_local(staged);
       }
@@ -490,52 +479,6 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
         const uint32_t src = src0 + pb * buf_bytes;
         const uint32_t end = src - vofs + 64u * min(ld_shared_u32(hdr_in + 64u * pb), qs);
         for (uint32_t at = src; at < end; at += step) apply_vector(c.slice, ld_shared_v4(at));
-      }
-    }
-
-    if constexpr (kHelper) {
-      // Mop-up (single-pass launches with a helper): the helper's tiles
-      // [cluster_tiles, ntiles) are claimed kMopTiles at a time from the
-      // counter the helper claims from, and each key goes straight to its
-      // owner (the pages' per-key DSMEM increment).  When the helper keeps
-      // pace this finds the counter spent at the first claim; when it falls
-      // behind (keys whose global atomics serialise), the clusters finish its
-      // share.  Each CTA claims on its own: the closing barrier below waits
-      // for all of them.  Thread 0 keeps the next claim in flight while the
-      // warps count the current one; it goes to slot j % 2 of the header,
-      // which every thread last read before the barrier of iteration j - 1.
-      const uint32_t slot0 = header0 + 224u;
-      const int4* hvec = vec + static_cast<size_t>(a.cluster_tiles) * 32u;
-      if (threadIdx.x == 0) {
-        const uint32_t first = atomicAdd(a.queue, kMopTiles);
-        st_shared_u32(slot0, first);
-        // The first CTA done with its rounds reports how the split went.
-        if (a.helper_report != nullptr && atomicCAS(a.queue + 1, 0u, 1u) == 0u)
-          report_helper_share(a.queue, a.helper_tiles, a.cluster_tiles, a.helper_report,
-                              a.helper_seq, first);
-      }
-      __syncthreads();
-      uint32_t t0 = ld_shared_u32(slot0);
-      for (uint32_t j = 1; t0 < a.helper_tiles; ++j) {
-        uint32_t next = 0;
-        if (threadIdx.x == 0) next = atomicAdd(a.queue, kMopTiles);
-        const uint32_t t1 = min(t0 + kMopTiles, a.helper_tiles);
-        for (uint32_t t = t0 + warp; t < t1; t += kWarps) {
-          const int4 v = ld_stream_v4(hvec + static_cast<size_t>(t) * 32u);
-          const int32_t keys[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint32_t rel = static_cast<uint32_t>(keys[u]) - c.base;
-            if (rel < c.range) {
-              uint32_t o, loc;
-              owner_local(rel, c, o, loc, kPow2);
-              red_add_cluster(map_rank(c.slice + 4u * loc, o), 1u);
-            }
-          }
-        }
-        if (threadIdx.x == 0) st_shared_u32(slot0 + 4u * (j & 1u), next);
-        __syncthreads();
-        t0 = ld_shared_u32(slot0 + 4u * (j & 1u));
       }
     }
 
@@ -641,6 +584,8 @@ __global__ void __launch_bounds__(kHelperThreads, 1) ship_helper_kernel(const Cl
   extern __shared__ __align__(16) uint32_t hc[];
   uint32_t* tags = hc;                  // key owning each slot (kNoKey: free)
   uint32_t* cnts = hc + kHelperSlots;   // its count
+  if (threadIdx.x == 0)  // the first CTA to start stamps the time (for the report)
+    atomicCAS(reinterpret_cast<unsigned long long*>(a.queue + 2), 0ull, global_timer_ns());
   for (uint32_t i = threadIdx.x; i < kHelperSlots; i += kHelperThreads) {
     tags[i] = kNoKey;
     cnts[i] = 0u;
@@ -687,17 +632,62 @@ __global__ void __launch_bounds__(kHelperThreads, 1) ship_helper_kernel(const Cl
     atomicExch(reinterpret_cast<unsigned long long*>(a.queue + 4), global_timer_ns());
 }
 
-template <int kKpt, bool kPow2, bool kSkew, bool kHelper = false>
-void* kernel_ptr_t() {
-  return reinterpret_cast<void*>(&cluster_ship_kernel<kKpt, kPow2, kSkew, kHelper>);
+// The mop-up, on the caller's stream right after the cluster kernel (whose
+// launch covered only its own tiles), beside the helper that may still run:
+// its first CTA reports how the split went, CTA 0 counts the ragged tail
+// after the last full tile, and every CTA claims kMopTiles tiles at a time
+// of the helper's range from the helper's counter (the next claim in flight
+// while its warps count the current one) and counts them into the helper's
+// row with global atomics.  When the helper has kept pace, each CTA's first
+// claim finds the range spent.  The cluster kernel itself carries none of
+// this: code after its rounds made the rounds compile 3-4% slower.
+__global__ void __launch_bounds__(kMopThreads) ship_mop_up_kernel(const ClusterHistArgs a,
+                                                                  uint32_t* row) {
+  __shared__ uint32_t s_claim[2];
+  constexpr uint32_t kMopWarps = kMopThreads / 32;
+  if (threadIdx.x == 0) {
+    if (a.helper_report != nullptr && atomicCAS(a.queue + 1, 0u, 1u) == 0u)
+      report_helper_share(a.queue, a.helper_tiles, a.cluster_tiles, a.helper_report, a.helper_seq,
+                          *reinterpret_cast<volatile uint32_t*>(a.queue));
+    s_claim[0] = atomicAdd(a.queue, kMopTiles);
+  }
+  const uint32_t ntiles = static_cast<uint32_t>(((a.n - a.head) >> 2) >> 5);
+  if (blockIdx.x == 0) {
+    const int64_t after = a.head + (static_cast<int64_t>(ntiles) << 7);
+    for (int64_t j = after + threadIdx.x; j < a.n; j += kMopThreads) {
+      const int32_t key = a.keys[j];
+      if (static_cast<uint32_t>(key) < a.num_bins) red_add_global(row + key, 1u);
+    }
+  }
+  __syncthreads();
+  const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+  const int4* hvec = reinterpret_cast<const int4*>(a.keys + a.head) + lane +
+                     static_cast<size_t>(a.cluster_tiles) * 32u;
+  uint32_t t0 = s_claim[0];
+  for (uint32_t j = 1; t0 < a.helper_tiles; ++j) {
+    // Slot j % 2 was last read after the barrier of iteration j - 2.
+    uint32_t next = 0;
+    if (threadIdx.x == 0) next = atomicAdd(a.queue, kMopTiles);
+    const uint32_t t1 = min(t0 + kMopTiles, a.helper_tiles);
+    for (uint32_t t = t0 + warp; t < t1; t += kMopWarps) {
+      const int4 v = ld_stream_v4(hvec + static_cast<size_t>(t) * 32u);
+      if (static_cast<uint32_t>(v.x) < a.num_bins) red_add_global(row + v.x, 1u);
+      if (static_cast<uint32_t>(v.y) < a.num_bins) red_add_global(row + v.y, 1u);
+      if (static_cast<uint32_t>(v.z) < a.num_bins) red_add_global(row + v.z, 1u);
+      if (static_cast<uint32_t>(v.w) < a.num_bins) red_add_global(row + v.w, 1u);
+    }
+    if (threadIdx.x == 0) s_claim[j & 1u] = next;
+    __syncthreads();
+    t0 = s_claim[j & 1u];
+  }
 }
 
-// The helper instantiations exist for 8 keys per thread only.
-void* ship_kernel_ptr(int kpt, bool pow2, bool skew, bool helper = false) {
-  if (helper) {
-    if (skew) return pow2 ? kernel_ptr_t<8, true, true, true>() : kernel_ptr_t<8, false, true, true>();
-    return pow2 ? kernel_ptr_t<8, true, false, true>() : kernel_ptr_t<8, false, false, true>();
-  }
+template <int kKpt, bool kPow2, bool kSkew>
+void* kernel_ptr_t() {
+  return reinterpret_cast<void*>(&cluster_ship_kernel<kKpt, kPow2, kSkew>);
+}
+
+void* ship_kernel_ptr(int kpt, bool pow2, bool skew) {
   if (skew) {
     if (kpt == 8) return pow2 ? kernel_ptr_t<8, true, true>() : kernel_ptr_t<8, false, true>();
     return pow2 ? kernel_ptr_t<4, true, true>() : kernel_ptr_t<4, false, true>();
@@ -718,8 +708,8 @@ cudaError_t read_and_clear_ship_status(uint32_t* out) {
 }
 
 cudaError_t prepare_ship_kernel(int kpt, int smem_bytes) {
-  for (int v = 0; v < (kpt == 8 ? 8 : 4); ++v) {
-    const void* fn = ship_kernel_ptr(kpt, (v & 1) != 0, (v & 2) != 0, (v & 4) != 0);
+  for (int v = 0; v < 4; ++v) {
+    const void* fn = ship_kernel_ptr(kpt, (v & 1) != 0, (v & 2) != 0);
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -768,31 +758,29 @@ cudaError_t launch_cluster_ship(const dsmem_hist_plan_t& plan, const ClusterHist
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const bool p2 = is_pow2(plan.bins_per_cta);
-  if (args.queue != nullptr) {  // beside the helper (8 keys per thread; the planner sees to it)
-    if (plan.keys_per_thread != 8) return cudaErrorInvalidValue;
-    if (args.hot_bin != kNoHot)
-      return p2 ? cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, true, true, true>, args)
-                : cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, false, true, true>, args);
-    return p2 ? cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, true, false, true>, args)
-              : cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, false, false, true>, args);
-  }
   if (args.hot_bin != kNoHot) {
     if (plan.keys_per_thread == 8)
-      return p2 ? cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, true, true, false>, args)
-                : cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, false, true, false>, args);
-    return p2 ? cudaLaunchKernelEx(&cfg, cluster_ship_kernel<4, true, true, false>, args)
-              : cudaLaunchKernelEx(&cfg, cluster_ship_kernel<4, false, true, false>, args);
+      return p2 ? cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, true, true>, args)
+                : cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, false, true>, args);
+    return p2 ? cudaLaunchKernelEx(&cfg, cluster_ship_kernel<4, true, true>, args)
+              : cudaLaunchKernelEx(&cfg, cluster_ship_kernel<4, false, true>, args);
   }
   if (plan.keys_per_thread == 8)
-    return p2 ? cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, true, false, false>, args)
-              : cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, false, false, false>, args);
-  return p2 ? cudaLaunchKernelEx(&cfg, cluster_ship_kernel<4, true, false, false>, args)
-            : cudaLaunchKernelEx(&cfg, cluster_ship_kernel<4, false, false, false>, args);
+    return p2 ? cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, true, false>, args)
+              : cudaLaunchKernelEx(&cfg, cluster_ship_kernel<8, false, false>, args);
+  return p2 ? cudaLaunchKernelEx(&cfg, cluster_ship_kernel<4, true, false>, args)
+            : cudaLaunchKernelEx(&cfg, cluster_ship_kernel<4, false, false>, args);
 }
 
 cudaError_t prepare_ship_helper() {
   return cudaFuncSetAttribute(ship_helper_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kHelperSmemBytes);
+}
+
+cudaError_t launch_ship_mop_up(const ClusterHistArgs& args, uint32_t* row, int ctas,
+                               cudaStream_t stream) {
+  ship_mop_up_kernel<<<static_cast<unsigned>(ctas), kMopThreads, 0, stream>>>(args, row);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_ship_helper(const ClusterHistArgs& args, uint32_t* row, int ctas,

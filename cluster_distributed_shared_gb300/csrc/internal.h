@@ -54,21 +54,21 @@ struct ClusterHistArgs {
   long long wait_cycles;    // bound of one inbox wait (clock64 cycles)
   uint32_t withhold_last;   // test only: senders skip the last round's arrival and stores
   uint32_t hot_bin;         // ship kernel: the plan's hot bin, 0xFFFFFFFF for none
-  // Ship kernel: its rounds cover tiles [0, cluster_tiles) (128 keys each,
-  // after `head`).  With a helper kernel beside it (single pass only),
-  // `queue` (zeroed before both launch) counts the claimed tiles of the
-  // helper's range [cluster_tiles, cluster_tiles + helper_tiles), which the
-  // cluster kernel's CTAs finish after their rounds; null without a helper.
+  // Helper and mop-up kernels (single-pass ship launches with a helper; the
+  // cluster kernel itself is launched on the first cluster_tiles tiles only,
+  // 128 keys each after `head`, and reads none of these): the helper's range
+  // is [cluster_tiles, cluster_tiles + helper_tiles), and `queue` (zeroed
+  // before the launches) counts its claimed tiles.
   uint32_t cluster_tiles;
   uint32_t helper_tiles;
   uint32_t* queue;
-  // With a helper: the first of this launch's CTAs to finish its rounds
-  // writes (helper_seq << 32) | (bits of a float: the helper's share at which
-  // both sides would have finished together) to this pinned, host-mapped
-  // word (may be null), from which the next launch on the stream sets the
-  // helper's share.  The zeroed kHelperQueueBytes at `queue`: u32 tile
-  // counter, u32 report flag, u64 globaltimer of the cluster kernel's start,
-  // u64 globaltimer of the helper kernel's end, u32 helper CTAs finished.
+  // The mop-up kernel's first CTA writes (helper_seq << 32) | (bits of a
+  // float: the helper's share at which both sides would have finished
+  // together) to this pinned, host-mapped word (may be null), from which the
+  // next launch on the stream sets the helper's share.  The zeroed
+  // kHelperQueueBytes at `queue`: u32 tile counter, u32 report flag, u64
+  // globaltimer of the helper's start, u64 globaltimer of its end, u32
+  // helper CTAs finished.
   unsigned long long* helper_report;
   uint32_t helper_seq;
 };
@@ -78,7 +78,7 @@ constexpr int64_t kHelperQueueBytes = 32;
 // claim, threads per CTA, the direct-mapped cache of frequent keys in its
 // shared memory (slots of a key and a count), and the fewest keys for which
 // a launch takes a helper.
-constexpr uint32_t kHelperTiles = 4;
+constexpr uint32_t kHelperTiles = 8;
 constexpr int kHelperThreads = 1024;
 constexpr int kHelperSlotsLog2 = 13;
 constexpr uint32_t kHelperSlots = 1u << kHelperSlotsLog2;
@@ -97,8 +97,10 @@ inline void set_partial_rows(dsmem_hist_plan_t* p, bool helper) {
                        (helper ? kHelperQueueBytes : 0);
 }
 
-// Tiles per claim of the ship kernel's mop-up: two per warp.
-constexpr uint32_t kMopTiles = 2 * (kShipThreads / 32);
+// The mop-up kernel after a ship launch with a helper: threads per CTA and
+// tiles per claim (two per warp).
+constexpr int kMopThreads = 512;
+constexpr uint32_t kMopTiles = 2 * (kMopThreads / 32);
 
 // Streams per device with their own status words (later streams share the
 // last slot).
@@ -122,6 +124,10 @@ cudaError_t launch_reduce_partials(const uint32_t* partials, uint64_t stride,
 // shared memory (prepare_ship_helper sets the limit once per device) count
 // the tiles of args' helper range they claim from args.queue into `row`.
 cudaError_t prepare_ship_helper();
+// The mop-up: `ctas` CTAs report the split, count the ragged tail, and
+// count the helper's tiles still unclaimed into `row`.
+cudaError_t launch_ship_mop_up(const ClusterHistArgs& args, uint32_t* row, int ctas,
+                               cudaStream_t stream);
 cudaError_t launch_ship_helper(const ClusterHistArgs& args, uint32_t* row, int ctas,
                                cudaStream_t stream);
 cudaError_t launch_global_atomic(const int32_t* keys, int64_t n, uint32_t num_bins,

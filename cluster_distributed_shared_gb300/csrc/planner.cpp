@@ -27,8 +27,8 @@
 //             fit kMaxAutoScratchBytes), at least 1
 //   helper  = one more partial row, for the global-atomic helper kernel on
 //             the SMs the clusters leave idle, when the plan is a
-//             single-pass SHIP plan with 8 keys per thread, of at least
-//             kHelperMinKeys keys, and at least kHelperMinIdleSms SMs stay idle
+//             single-pass SHIP plan of at least kHelperMinKeys keys and at
+//             least kHelperMinIdleSms SMs stay idle
 #include <stdint.h>
 
 #include "internal.h"
@@ -221,8 +221,8 @@ int plan_shape(const dsmem_hist_device_t* dev, int32_t num_bins, int64_t n,
   }
   out->partial_stride = stride;
   const int64_t idle = static_cast<int64_t>(dev->sm_count) - C * P;
-  const bool helper = kernel == DSMEM_HIST_KERNEL_SHIP && passes == 1 && kpt == 8 &&
-                      n >= kHelperMinKeys && idle >= kHelperMinIdleSms;
+  const bool helper = kernel == DSMEM_HIST_KERNEL_SHIP && passes == 1 && n >= kHelperMinKeys &&
+                      idle >= kHelperMinIdleSms;
   set_partial_rows(out, helper);
   return DSMEM_HIST_OK;
 }
