@@ -553,7 +553,8 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
 // warps claim kHelperTiles tiles at a time of the tiles after the clusters'
 // rounds, [cluster_tiles, cluster_tiles + helper_tiles), from the counter
 // the clusters' mop-up claims from (the next claim in flight while the
-// current one is counted), and count each in-range key into the helper's
+// current one is counted, kHelperBatch tiles loaded at a time), and count
+// each in-range key into the helper's
 // partial row: with a global atomic, the comparison kernel's method
 // ("Distributed Shared Memory", section "When it beats global atomics"),
 // unless the key owns its slot of a direct-mapped cache in shared memory
@@ -599,24 +600,26 @@ __global__ void __launch_bounds__(kHelperThreads, 1) ship_helper_kernel(const Cl
   uint32_t t0 = __shfl_sync(kFullMask, mine, 0);
   while (t0 < a.helper_tiles) {
     if (lane == 0) mine = atomicAdd(a.queue, kHelperTiles);  // the next claim
-    int4 v[kHelperTiles];
+    for (uint32_t bt = t0; bt < t0 + kHelperTiles; bt += kHelperBatch) {
+      int4 v[kHelperBatch];
 #pragma unroll
-    for (uint32_t u = 0; u < kHelperTiles; ++u)
-      v[u] = t0 + u < a.helper_tiles ? ld_stream_v4(hvec + static_cast<size_t>(t0 + u) * 32u)
-                                     : make_int4(-1, -1, -1, -1);
+      for (uint32_t u = 0; u < kHelperBatch; ++u)
+        v[u] = bt + u < a.helper_tiles ? ld_stream_v4(hvec + static_cast<size_t>(bt + u) * 32u)
+                                       : make_int4(-1, -1, -1, -1);
 #pragma unroll
-    for (uint32_t u = 0; u < kHelperTiles; ++u) {
-      // A tile of 128 equal keys (runs) is one atomic of 128.
-      const int32_t k0 = __shfl_sync(kFullMask, v[u].x, 0);
-      const bool eq = (v[u].x == k0) & (v[u].y == k0) & (v[u].z == k0) & (v[u].w == k0);
-      if (__all_sync(kFullMask, eq)) {
-        if (lane == 0 && static_cast<uint32_t>(k0) < a.num_bins) red_add_global(row + k0, 128u);
-        continue;
+      for (uint32_t u = 0; u < kHelperBatch; ++u) {
+        // A tile of 128 equal keys (runs) is one atomic of 128.
+        const int32_t k0 = __shfl_sync(kFullMask, v[u].x, 0);
+        const bool eq = (v[u].x == k0) & (v[u].y == k0) & (v[u].z == k0) & (v[u].w == k0);
+        if (__all_sync(kFullMask, eq)) {
+          if (lane == 0 && static_cast<uint32_t>(k0) < a.num_bins) red_add_global(row + k0, 128u);
+          continue;
+        }
+        helper_count(v[u].x, a.num_bins, tags, cnts, row);
+        helper_count(v[u].y, a.num_bins, tags, cnts, row);
+        helper_count(v[u].z, a.num_bins, tags, cnts, row);
+        helper_count(v[u].w, a.num_bins, tags, cnts, row);
       }
-      helper_count(v[u].x, a.num_bins, tags, cnts, row);
-      helper_count(v[u].y, a.num_bins, tags, cnts, row);
-      helper_count(v[u].z, a.num_bins, tags, cnts, row);
-      helper_count(v[u].w, a.num_bins, tags, cnts, row);
     }
     t0 = __shfl_sync(kFullMask, mine, 0);
   }

@@ -75,10 +75,12 @@ struct ClusterHistArgs {
 constexpr int64_t kHelperQueueBytes = 32;
 
 // The global-atomic helper on the SMs a ship launch leaves idle: tiles per
-// claim, threads per CTA, the direct-mapped cache of frequent keys in its
-// shared memory (slots of a key and a count), and the fewest keys for which
-// a launch takes a helper.
-constexpr uint32_t kHelperTiles = 8;
+// claim and tiles loaded at a time (a claim counted in two batches gives the
+// next claim twice as long to return), threads per CTA, the direct-mapped
+// cache of frequent keys in its shared memory (slots of a key and a count),
+// and the fewest keys for which a launch takes a helper.
+constexpr uint32_t kHelperTiles = 16;
+constexpr uint32_t kHelperBatch = 8;
 constexpr int kHelperThreads = 1024;
 constexpr int kHelperSlotsLog2 = 13;
 constexpr uint32_t kHelperSlots = 1u << kHelperSlotsLog2;
