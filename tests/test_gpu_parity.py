@@ -570,6 +570,66 @@ def test_idle_sm_helper_and_mop_up(monkeypatch, mode, share):
     assert pkg.dsmem_hist_device_status() == 0
 
 
+@pytest.mark.parametrize("seed", [4242, 777])
+def test_helper_randomized_streams(seed):
+    """Seeded random launches that take the idle-SM helper (single-pass
+    plans of clusters of 8 or 16 with at least 2^24 keys), issued back to back
+    on three streams with no synchronisation between them, so that helpers,
+    mop-ups and share reports of neighbouring launches overlap: random bin
+    counts, lengths with ragged tails, misaligned starts, key mixes (uniform,
+    Zipf, runs, one hot bin, out-of-range keys), the product call and the two
+    stages (accumulating); every result bit-exact against the oracle."""
+    rng = np.random.default_rng(seed)
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    shapes = [(8192, 8), (100003, 8), (200000, 8), (262144, 8), (262144, 0), (300007, 16),
+              (524288, 16)]
+    trials = []
+    for trial in range(21):
+        num_bins, P = shapes[trial % len(shapes)]
+        n = (1 << 24) + int(rng.integers(0, 1 << 22))
+        off = int(rng.integers(0, 4))
+        kseed = seed + 500 + trial
+        mix = int(rng.integers(0, 5))
+        if mix == 0:
+            keys = gen.uniform(n + off, num_bins, seed=kseed)
+        elif mix == 1:
+            keys = gen.zipf(n + off, num_bins, seed=kseed)
+        elif mix == 2:
+            keys = gen.runs(n + off, num_bins, seed=kseed)
+        elif mix == 3:
+            keys = gen.hot(n + off, num_bins, seed=kseed)
+        else:
+            keys = gen.uniform(n + off, num_bins + num_bins // 4, seed=kseed) - num_bins // 8
+        keys = np.ascontiguousarray(keys, np.int32)
+        plan = pkg.dsmem_hist_plan(num_bins, n, **({"cluster_size": P} if P else {}))
+        assert plan["passes"] == 1 and plan["partial_rows"] == plan["num_clusters"] + 1, plan
+        trials.append((trial, num_bins, P, off, keys, plan))
+    dev = [torch.from_numpy(t[4]).cuda() for t in trials]
+    torch.cuda.synchronize()                 # keys uploaded before the side streams read them
+    results = []
+    for (trial, num_bins, P, off, keys, plan), d in zip(trials, dev):
+        s = streams[trial % len(streams)]
+        sub = d[off:]
+        kw = {"cluster_size": P} if P else {}
+        if trial % 3 == 2:                   # the two stages, the second accumulating
+            partials = torch.empty(-(-plan["workspace_bytes"] // 4), dtype=torch.int32,
+                                   device="cuda")
+            cut = int(rng.integers(1, sub.numel()))
+            pkg.dsmem_hist_partials(sub[:cut], num_bins, plan, partials, 0, stream=s)
+            pkg.dsmem_hist_partials(sub[cut:], num_bins, plan, partials, 1, stream=s)
+            got = pkg.dsmem_hist_reduce(partials, plan["partial_rows"], plan["partial_stride"],
+                                        num_bins, stream=s)
+            results.append((got, partials))
+        else:
+            results.append((pkg.dsmem_hist(sub, num_bins, stream=s, **kw), None))
+    torch.cuda.synchronize()
+    for (trial, num_bins, P, off, keys, plan), (got, _) in zip(trials, results):
+        want = oracle.histogram(keys[off:], num_bins)
+        g = to_np(got)
+        assert np.array_equal(g, want), (trial, num_bins, P, off, np.flatnonzero(g != want)[:8])
+    assert pkg.dsmem_hist_device_status() == 0
+
+
 _SHARE_SCRIPT = r"""
 import sys, numpy as np, torch
 sys.path.insert(0, sys.argv[1])
