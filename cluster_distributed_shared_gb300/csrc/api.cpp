@@ -329,9 +329,9 @@ constexpr double kHelperGainMin = 0.05, kHelperGainMax = 0.75;
 
 // The helper's share for the next launch on the stream of `sr`: the share it
 // has learned, else `prior`.  Each launch with a helper reports, from the
-// first CTA done with its rounds, the share at which the helper and the
+// mop-up kernel's first CTA, the share at which the helper and the
 // clusters would have finished together (report_helper_share in the ship
-// kernel); a new report moves the share part of the way to it.  The step
+// kernel's source); a new report moves the share part of the way to it.  The step
 // starts at three quarters, halves (down to kHelperGainMin) whenever the
 // correction changes direction and grows again by a quarter while it keeps
 // its direction: where the helper's pace depends on which tiles it gets
@@ -387,9 +387,9 @@ double helper_share(DeviceState* st, const SlotRef* sr, int kind, double prior) 
 // takes the rest: its share starts at what the idle SMs would finish in the
 // time the clusters take for theirs and then follows the stream's reports
 // (helper_share); the clusters' tiles are rounded down to whole rounds.
-// The helper runs on a second stream forked from and joined back into
-// `stream`; the tile counter is zeroed on `stream` before the fork and the
-// helper's row on the helper stream (unless accumulating).  The mop-up
+// The cluster kernel and the helper run on two library streams forked from
+// and joined back into `stream`; the tile counter and (unless accumulating)
+// the helper's row are zeroed on `stream` before the fork.  The mop-up
 // kernel follows the cluster kernel on `stream`.
 cudaError_t launch_plan(const dsmem_hist_plan_t& plan, ClusterHistArgs args, cudaStream_t stream,
                         DeviceState* st = nullptr, const SlotRef* sr = nullptr) {

@@ -552,7 +552,7 @@ __global__ void __launch_bounds__(kShipThreads, 1) cluster_ship_kernel(const Clu
 // leave idle (clusters of 8 fit only 15 times into this GPU's 152 SMs).  Its
 // warps claim kHelperTiles tiles at a time of the tiles after the clusters'
 // rounds, [cluster_tiles, cluster_tiles + helper_tiles), from the counter
-// the clusters' mop-up claims from (the next claim in flight while the
+// the mop-up kernel claims from (the next claim in flight while the
 // current one is counted, kHelperBatch tiles loaded at a time), and count
 // each in-range key into the helper's
 // partial row: with a global atomic, the comparison kernel's method
@@ -628,8 +628,8 @@ __global__ void __launch_bounds__(kHelperThreads, 1) ship_helper_kernel(const Cl
     const uint32_t n = cnts[i];
     if (n != 0u) red_add_global(row + tags[i], n);
   }
-  // The last CTA to finish stamps the time (for the report in the cluster
-  // kernel's mop-up).
+  // The last CTA to finish stamps the time (for the report of the mop-up
+  // kernel).
   __syncthreads();
   if (threadIdx.x == 0 && atomicAdd(a.queue + 6, 1u) == gridDim.x - 1u)
     atomicExch(reinterpret_cast<unsigned long long*>(a.queue + 4), global_timer_ns());

@@ -210,12 +210,12 @@ DSMEM_HIST_API int dsmem_hist_host(const int32_t* h_keys, int64_t n, int32_t num
  * stream of the library forked from and joined back into `stream`: the
  * clusters' rounds take the first tiles of the keys, the helper the rest
  * ("When it beats global atomics": one global atomic per key, into the last
- * row), and clusters that finish early take the helper's tiles it has not
- * claimed yet.  The helper's share of the tiles starts from the idle SMs'
- * expected pace and then follows what earlier launches on the same stream
- * report: the first cluster CTA done with its rounds computes, from the
- * GPU's global timer, the share at which both sides would have finished
- * together.  DSMEM_HIST_HELPER=0 in the environment makes the planner leave
+ * row), and a small mop-up kernel after the cluster kernel takes the
+ * helper's tiles it has not claimed yet.  The helper's share of the tiles
+ * starts from the idle SMs' expected pace and then follows what earlier
+ * launches on the same stream report: the mop-up kernel's first CTA computes,
+ * from the GPU's global timer, the share at which both sides would have
+ * finished together.  DSMEM_HIST_HELPER=0 in the environment makes the planner leave
  * the helper out.
  *   plan      from dsmem_hist_plan for the same num_bins (checked for
  *             consistency; EINVAL otherwise)

@@ -531,10 +531,10 @@ def test_hot_bin_kernel_is_chosen_from_the_previous_histogram():
                                         ("1", "1")])
 def test_idle_sm_helper_and_mop_up(monkeypatch, mode, share):
     """Clusters of 8 leave 32 SMs idle; a global-atomic helper kernel on them
-    takes the tiles after the clusters' rounds, and clusters that finish
-    early take the ones it has not claimed.  Exact with the helper off, at
-    its planned share, with no tiles for it, with half and with all of them
-    (the clusters' mop-up then does much of the work): on uniform, Zipf and
+    takes the tiles after the clusters' rounds, and a mop-up kernel after the
+    cluster kernel takes the ones it has not claimed.  Exact with the helper
+    off, at its planned share, with no tiles for it, with half and with all
+    of them (the mop-up then does much of the work): on uniform, Zipf and
     run-heavy keys, at a pointer offset, through the product call, the
     two-stage entry points (accumulating too) and the host entry point."""
     monkeypatch.setenv("DSMEM_HIST_HELPER", mode)
