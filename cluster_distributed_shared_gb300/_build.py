@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(PKG, "libdsmemhist.so")
 SOURCES = ["cluster_hist.cu", "cluster_ship.cu", "static_scratch.cu", "microbench.cu", "planner.cpp",
            "api.cpp"]
 HEADERS = [os.path.join(CSRC, "internal.h"), os.path.join(CSRC, "ptx.cuh"),
-           os.path.join(INCLUDE, "dsmem_hist.h")]
+           os.path.join(CSRC, "helper_split.h"), os.path.join(INCLUDE, "dsmem_hist.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-Wall,-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC]

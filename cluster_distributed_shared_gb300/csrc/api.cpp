@@ -19,6 +19,7 @@
 #include <cuda_runtime_api.h>
 
 #include "dsmem_hist.h"
+#include "helper_split.h"
 #include "internal.h"
 
 namespace dsmh {
@@ -69,18 +70,11 @@ struct DeviceState {
   HelperStream helper_streams[kStatusSlots + 1] = {};
   bool helper_prepared = false;
   std::mutex helper_call;
-  // Per stream slot, under helper_call: the helper's current share of the
-  // tiles beside the default and beside the hot-bin kernel (0: none learned
-  // yet; the best shares differ), the last report taken, and the last
-  // sequence number handed out (2 * launch count + kind).
-  double helper_share[kStatusSlots][2] = {};
-  // The step towards a report (0: not started), and the sign of the last
-  // correction, per slot and kind.
-  double helper_gain[kStatusSlots][2] = {};
-  int helper_last_sign[kStatusSlots][2] = {};
-  // The first launch (count) that ran with the current share, per slot and
-  // kind: reports of earlier launches describe an older share.
-  uint32_t helper_valid_from[kStatusSlots][2] = {};
+  // Per stream slot, under helper_call: the helper's learned share beside
+  // the default and beside the hot-bin kernel (the best shares differ), the
+  // last report taken, and the last sequence number handed out (2 * launch
+  // count + kind).
+  HelperShare helper[kStatusSlots][2] = {};
   uint32_t helper_taken[kStatusSlots] = {};
   uint32_t helper_seq[kStatusSlots] = {};
   // Per-stream words in pinned, host-mapped memory (h_status on the host,
@@ -320,65 +314,33 @@ int prepare_locked(DeviceState* st, const dsmem_hist_plan_t& p) {
   return DSMEM_HIST_OK;
 }
 
-// The helper's speed per idle SM relative to a cluster SM's (global atomics
-// against the ship kernel, measured on uniform keys); it sets the helper's
-// share of the tiles until a stream has reported how the split went.
-constexpr double kHelperRelativeRate = 0.42;
-constexpr double kHelperShareMin = 0.01, kHelperShareMax = 0.6;
-constexpr double kHelperGainMin = 0.05, kHelperGainMax = 0.75;
-
 // The helper's share for the next launch on the stream of `sr`: the share it
 // has learned, else `prior`.  Each launch with a helper reports, from the
 // mop-up kernel's first CTA, the share at which the helper and the
 // clusters would have finished together (report_helper_share in the ship
-// kernel's source); a new report moves the share part of the way to it.  The step
-// starts at three quarters, halves (down to kHelperGainMin) whenever the
-// correction changes direction and grows again by a quarter while it keeps
-// its direction: where the helper's pace depends on which tiles it gets
-// (runs in the last half of the keys and uniform keys before them: the
-// reported target then moves several times as far as the share), full steps
-// made the share swing around its optimum by a quarter.  Shares are kept
+// kernel's source); a new report of a launch made at the current share moves
+// the share part of the way to it (helper_share_step).  Shares are kept
 // apart for the default (kind 0) and the hot-bin kernel (kind 1); a report's
 // sequence number carries its kind in bit 0 and the launch count above it.
-// A report counts only if its launch ran with the current share: calls
-// enqueued far ahead of the GPU see reports of launches made with an older
-// share, and acting on those made the share overshoot.  st->helper_call
-// must be held.
+// st->helper_call must be held.
 double helper_share(DeviceState* st, const SlotRef* sr, int kind, double prior) {
   if (!sr || sr->slot < 0 || !sr->h_helper) return prior;
   const int slot = sr->slot;
-  for (double& s : st->helper_share[slot])
-    if (s <= 0.0) s = prior;
+  for (HelperShare& h : st->helper[slot])
+    if (h.share <= 0.0) h.share = prior;
   const unsigned long long w = *reinterpret_cast<volatile unsigned long long*>(sr->h_helper);
   const uint32_t seq = static_cast<uint32_t>(w >> 32), bits = static_cast<uint32_t>(w);
-  const uint32_t k = seq & 1u;
-  if (seq != 0 && seq != st->helper_taken[slot] &&
-      static_cast<int32_t>((seq >> 1) - st->helper_valid_from[slot][k]) >= 0) {
+  HelperShare& h = st->helper[slot][seq & 1u];
+  if (seq != 0 && seq != st->helper_taken[slot] && helper_report_current(h, seq >> 1)) {
     st->helper_taken[slot] = seq;
-    double& share = st->helper_share[slot][k];
-    double& gain = st->helper_gain[slot][k];
-    int& last_sign = st->helper_last_sign[slot][k];
     float target = 0.0f;
     memcpy(&target, &bits, sizeof target);
-    if (target > 0.0f && target < 1.0f) {
-      const double before = share;
-      const int sign = target > share ? 1 : -1;
-      if (gain <= 0.0)
-        gain = kHelperGainMax;
-      else if (last_sign != 0 && sign != last_sign)
-        gain = gain * 0.5 < kHelperGainMin ? kHelperGainMin : gain * 0.5;
-      else
-        gain = gain * 1.25 > kHelperGainMax ? kHelperGainMax : gain * 1.25;
-      last_sign = sign;
-      share += gain * (target - share);
-      share = share < kHelperShareMin ? kHelperShareMin : (share > kHelperShareMax ? kHelperShareMax : share);
-      if (share != before) st->helper_valid_from[slot][k] = (st->helper_seq[slot] >> 1) + 1u;
-      if (trace_enabled())
-        fprintf(stderr, "[dsmem_hist] stream slot %d: helper launch %u (kind %u) reports share %.4f "
-                "-> share %.4f -> %.4f\n", slot, seq >> 1, seq & 1u, target, before, share);
-    }
+    const double before = h.share;
+    if (helper_share_step(h, target, st->helper_seq[slot] >> 1) && trace_enabled())
+      fprintf(stderr, "[dsmem_hist] stream slot %d: helper launch %u (kind %u) reports share %.4f "
+              "-> share %.4f -> %.4f\n", slot, seq >> 1, seq & 1u, target, before, h.share);
   }
-  return st->helper_share[slot][kind];
+  return st->helper[slot][kind].share;
 }
 
 // Launches a plan.  With `st` non-null and a helper row in the plan
@@ -420,12 +382,10 @@ cudaError_t launch_plan(const dsmem_hist_plan_t& plan, ClusterHistArgs args, cud
   const int active = plan.num_clusters * plan.cluster_size;
   const int idle = st->dev.sm_count > active ? st->dev.sm_count - active : 0;
   const int kind = args.hot_bin != 0xFFFFFFFFu ? 1 : 0;
-  double share = helper_share(st, sr, kind, idle * kHelperRelativeRate / (active + idle * kHelperRelativeRate));
+  double share = helper_share(st, sr, kind, helper_prior(active, idle));
   if (const char* v = getenv("DSMEM_HIST_HELPER_SHARE")) share = atof(v);  // sweeps
-  share = share < 0.0 ? 0.0 : (share > 1.0 ? 1.0 : share);
   const uint64_t per_round = static_cast<uint64_t>(active) * (kShipThreads / 32) * (plan.keys_per_thread / 4);
-  args.cluster_tiles = static_cast<uint32_t>(
-      static_cast<uint64_t>(static_cast<double>(ntiles) * (1.0 - share)) / per_round * per_round);
+  args.cluster_tiles = helper_cluster_tiles(ntiles, share, per_round);
   args.helper_tiles = ntiles - args.cluster_tiles;
   uint32_t* row = args.partials + static_cast<size_t>(plan.num_clusters) * args.stride;
   args.queue = args.partials + static_cast<size_t>(plan.partial_rows) * args.stride;

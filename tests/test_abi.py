@@ -73,6 +73,27 @@ def test_header_compiles_as_c_and_links(tmp_path):
     assert f"block_threads={pkg.SHIP_THREADS}" in out.stdout
 
 
+def test_helper_split_controller(tmp_path):
+    # tests/helper_split_check.cpp drives the idle-SM helper's share
+    # controller and tile split (csrc/helper_split.h, the code the library's
+    # launcher runs) with synthetic reports: prior, convergence without
+    # overshoot, clamps, ignored targets, damping on direction changes, the
+    # stale-report window (with wrap-around), whole-round splits.
+    import shutil
+    import subprocess
+    gxx = shutil.which("g++")
+    if gxx is None:
+        pytest.skip("no g++")
+    exe = str(tmp_path / "helper_split_check")
+    cmd = [gxx, "-std=c++17", "-O2", "-Wall", "-Wextra", "-Werror",
+           "-I", os.path.join(ROOT, "cluster_distributed_shared_gb300", "csrc"),
+           os.path.join(ROOT, "tests", "helper_split_check.cpp"), "-o", exe]
+    subprocess.run(cmd, check=True, capture_output=True, text=True)
+    out = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, out.stdout + out.stderr
+    assert out.stdout.strip() == "ok"
+
+
 def test_version_and_strerror():
     assert pkg.dsmem_hist_version() >= 100
     for code in (0, -1, -2, -3, -4, -5):
